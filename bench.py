@@ -1,0 +1,424 @@
+"""Benchmark of split-K paged-attention decode on GB300.
+
+Prints ONE JSON line (rank 0).  A step is one decode call over one batch of
+the workload: phase 1 (attention over every partition) and phase 2 (the
+log-sum-exp merge) for V2, or the single pass for V1 -- whichever the V1/V2
+dispatch picks for the workload.  The metric is effective KV-read bandwidth:
+the K and V bytes a decode must read (sum over sequences of
+seq_len * num_kv_heads * head_dim * 2 * 2 bytes) divided by the time per call.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                        [--impl reference]
+Under torchrun (N > 1) every rank decodes its own replica of the workload
+(no data exchange: the path has none) and the slowest rank's time is used.
+``--impl reference`` times the fp64 CPU oracle instead, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "paged-decode attention effective KV-read GB/s (% of HBM peak); µs per call"
+DEFAULT_CONFIG = "batch_decode"
+KERNEL_SOURCES = ["paged_kv_decode_v2_gb300/csrc/pa_attn.cuh",
+                  "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"]
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world <= 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[f"{kernel}/{workload}"]
+    except Exception:
+        return None
+    if rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- the CUDA path
+
+class Decoder:
+    """One workload on one GPU: inputs (rotated copies when small vs L2) and workspace."""
+
+    def __init__(self, w: wl.Workload, device):
+        import paged_kv_decode_v2_gb300 as pa
+        self.pa = pa
+        pa.load()
+        self.w = w
+        self.device = device
+        base = wl.make_inputs(w, device=device)
+        self.kv_bytes = base.kv_bytes
+        # Inputs larger than L2 between reuses: rotate through R copies of the caches.
+        self.copies = max(1, math.ceil(3 * L2_BYTES / max(1, self.kv_bytes)))
+        self.caches = [(base.key_cache, base.value_cache)]
+        for r in range(1, self.copies):
+            g = torch.Generator(device=device).manual_seed(w.seed + 100 + r)
+            k = torch.randn(base.key_cache.shape, generator=g, device=device).to(base.key_cache.dtype)
+            v = torch.randn(base.value_cache.shape, generator=g, device=device).to(base.value_cache.dtype)
+            self.caches.append((k, v))
+        self.inp = base
+        S, H, D = base.query.shape
+        self.cap = base.block_tables.shape[1] * w.block_size
+        self.max_seq_len = base.max_seq_len
+        self.np = pa.num_partitions(self.max_seq_len, w.partition_size)
+        self.tmp, self.es, self.ml = pa.alloc_workspace(S, H, D, max(1, self.np), device=device)
+        self.out = torch.empty_like(base.query)
+        self.variant = pa.pa_decode_choose(S, w.num_kv_heads, self.max_seq_len, w.partition_size)
+        self.launches_per_step = 2 if self.variant == 2 else 1
+
+    def step(self, i: int, ev=None):
+        """One decode call on copy i % R.  ev = (start, mid, end) events to record, or None."""
+        pa, w, inp = self.pa, self.w, self.inp
+        kc, vc = self.caches[i % self.copies]
+        if ev is not None:
+            ev[0].record()
+        if self.variant == 2:
+            pa.pa_decode_v2_phase1(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
+                                   w.partition_size, self.tmp, self.es, self.ml,
+                                   max_seq_len_hint=self.max_seq_len)
+            if ev is not None:
+                ev[1].record()
+            pa.pa_decode_v2_phase2(inp.seq_lens, self.max_seq_len, w.partition_size, self.tmp,
+                                   self.es, self.ml, self.out)
+        else:
+            pa.pa_decode_v1(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, self.out,
+                            max_seq_len_hint=self.max_seq_len)
+            if ev is not None:
+                ev[1].record()
+        if ev is not None:
+            ev[2].record()
+
+    def e2e_step(self, i: int, host):
+        """Host buffers in, host result out: H2D of this step's inputs, decode, D2H of out."""
+        pa, w = self.pa, self.w
+        q_h, bt_h, sl_h, out_h = host
+        inp = self.inp
+        inp.query.copy_(q_h, non_blocking=True)
+        inp.block_tables.copy_(bt_h, non_blocking=True)
+        inp.seq_lens.copy_(sl_h, non_blocking=True)
+        kc, vc = self.caches[i % self.copies]
+        pa.pa_decode(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, w.partition_size,
+                     self.out, self.tmp, self.es, self.ml, max_seq_len_hint=self.max_seq_len)
+        out_h.copy_(self.out, non_blocking=True)
+
+
+def time_gpu(args, w: wl.Workload):
+    world, rank, local = dist_env()
+    init_dist(world, "nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    dec = Decoder(w, device)
+    K, W = args.steps, args.warmup
+
+    for i in range(W):
+        dec.step(i)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(local) as clk:
+        # keep the GPU loaded around the timed region so the clock samples describe it
+        t_end = time.time() + 1.0
+        i = W
+        while time.time() < t_end:
+            dec.step(i)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for k in range(K):
+            dec.step(i + k, evs[k])
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        t_end = time.time() + 0.5
+        j = i + K
+        while time.time() < t_end:
+            dec.step(j)
+            j += 1
+            if j % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+
+    total_ms = t0.elapsed_time(t1)
+    k1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    k2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    total_ms = max_over_ranks(total_ms, world, device)
+    ms_step = total_ms / K
+
+    # end to end through the public API with host buffers
+    q_h = dec.inp.query.cpu().pin_memory()
+    bt_h = dec.inp.block_tables.cpu().pin_memory()
+    sl_h = dec.inp.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(dec.out.shape, dtype=dec.out.dtype).pin_memory()
+    host = (q_h, bt_h, sl_h, out_h)
+    for i in range(W):
+        dec.e2e_step(i, host)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(K):
+        dec.e2e_step(k, host)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / K
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+
+    gbs = world * dec.kv_bytes / (ms_step * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+    kernel = "pa_attn_v2_phase1" if dec.variant == 2 else "pa_attn_v1"
+    k1_gbs = dec.kv_bytes / (k1_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(w.name, kernel)
+    result = {
+        "metric": METRIC,
+        "value": round(gbs, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_step, 6),
+        "us_per_call": round(ms_step * 1e3, 3),
+        "pct_of_hbm_peak": round(100.0 * gbs / world / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.DTYPE_NAME[w.dtype],
+        "data": "synthetic (seeded N(0,1) queries and paged K/V caches, random block placement)",
+        "config": {
+            "workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "partition_size": w.partition_size, "max_seq_len": dec.max_seq_len,
+            "sum_seq_len": int(dec.inp.seq_lens.sum().item()), "kv_bytes_per_step": dec.kv_bytes,
+            "variant": f"v{dec.variant}", "accumulate": "f32",
+            "l2": (f"inputs larger than L2: {dec.copies} rotating K/V cache copies, "
+                   f"{dec.copies * dec.kv_bytes / 1e6:.0f} MB read between reuses vs 129 MB L2"),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "e2e": {"value": round(world * dec.kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * dec.launches_per_step,
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(k1_gbs / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dec.kv_bytes,
+                     "kernel_us": round(k1_ms * 1e3, 3),
+                     "merge_us": round(k2_ms * 1e3, 3) if dec.variant == 2 else None},
+        "clocks": clocks,
+    }
+    return result, dec, rank, world
+
+
+# ---------------------------------------------------------------- the oracle on the host
+
+def time_oracle(w: wl.Workload, budget_s: float = 12.0):
+    """The fp64 oracle as it stands, on all host cores, over a bounded sample of the workload."""
+    import oracle
+    inp = wl.make_inputs(w, device="cpu")
+    prob = oracle.Problem.from_arrays(wl.to_oracle_arrays(inp))
+    cores = os.cpu_count() or 1
+    S, H = w.num_seqs, w.num_heads
+    order = list(range(S * H))
+    # grow the sample of (seq, head) pairs until one pass takes a noticeable time
+    n = max(1, min(len(order), 64))
+    while True:
+        pairs = [(i // H, i % H) for i in order[:n]]
+        t = time.perf_counter()
+        oracle.decode(prob, pairs=pairs, num_threads=cores)
+        dt = time.perf_counter() - t
+        if dt > budget_s / 4 or n == len(order):
+            break
+        n = min(len(order), n * 4)
+    reps = max(1, int(budget_s / max(dt, 1e-3) / 2))
+    t = time.perf_counter()
+    for _ in range(reps):
+        oracle.decode(prob, pairs=pairs, num_threads=cores)
+    dt = (time.perf_counter() - t) / reps
+    lens = inp.seq_lens.tolist()
+    sample_bytes = sum(lens[b] * w.head_dim * 2 * 2 for b, h in pairs) // w.group_size
+    gbs = sample_bytes / dt / 1e9
+    desc = (f"{len(pairs)} of {S * H} (seq, head) pairs of {w.name}"
+            f"{' (all)' if len(pairs) == S * H else ''}, {reps} timed passes of {dt:.2f} s")
+    return gbs, cores, desc, dt * (S * H) / len(pairs)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.ALL))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = wl.ALL[args.config]
+    world, rank, _ = dist_env()
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        gbs, cores, desc, full_s = time_oracle(w)
+        line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(full_s * 1e3, 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "impl": "reference",
+                "config": {"workload": w.name},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    result, dec, rank, world = time_gpu(args, w)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            gbs, cores, desc, _ = time_oracle(w)
+            result["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores,
+                                      "kind": "oracle", "sample": desc}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,223 @@
+/*
+ * pa_decode.h -- C ABI of the split-K paged-attention decode library
+ * (libpa_decode.so, CUDA for sm_103a).
+ *
+ * Operation (what every entry point computes)
+ * -------------------------------------------
+ * For each sequence b < num_seqs and query head h < num_heads, with
+ * G = num_heads / num_kv_heads and KV head k = h / G (one KV head serves a
+ * contiguous group of G query heads -- the GQA broadcast of the
+ * "paged_attention_v2_pytorch.py" commit 15ef28e, "Key changes"):
+ *
+ *     K_t = key_cache  [block_tables[b][t / block_size], k, t % block_size, :]
+ *     V_t = value_cache[block_tables[b][t / block_size], k, t % block_size, :]
+ *     s_t = scale * <query[b, h, :], K_t>                  for t < seq_lens[b]
+ *     out[b, h, :] = sum_t softmax(s)_t * V_t
+ *
+ * pa_decode_v2 computes it in the two passes of the pages' "V2"
+ * ("paged_attention_v2_pytorch.py" commit 9cb7f9d, "Implementation"):
+ *   phase 1, per (sequence, head, partition p of partition_size tokens):
+ *       max_logits[b,h,p] = m_p = max_{t in p} s_t
+ *       exp_sums  [b,h,p] = l_p = sum_{t in p} exp(s_t - m_p)
+ *       tmp_output[b,h,p,:] = o_p = sum_{t in p} exp(s_t - m_p) V_t / l_p
+ *   phase 2, per (sequence, head), the log-sum-exp merge:
+ *       M = max_p m_p,  w_p = exp(m_p - M) * l_p,
+ *       out[b,h,:] = sum_p (w_p / sum_q w_q) * o_p
+ * over the ceil(seq_lens[b] / partition_size) partitions of sequence b.
+ * pa_decode_v1 is the single-pass form (one CTA per (sequence, KV head)
+ * walks every block with a running {m, l, o}; "vllm/_custom_ops.py" commit
+ * 900ae0b, "V1: 1 CTA iterates ... partitions sequentially").  pa_decode
+ * chooses between them ("paged_attn.py" commit 490ff98, change 1: restore
+ * the V1/V2 adaptive dispatch), with a rule re-derived for this GPU.
+ *
+ * Layouts (all row-major, contiguous, device memory)
+ * --------------------------------------------------
+ *   query        [num_seqs, num_heads, head_dim]                 dtype
+ *   key_cache    [num_blocks, num_kv_heads, block_size, head_dim] dtype
+ *   value_cache  [num_blocks, num_kv_heads, block_size, head_dim] dtype
+ *   block_tables [num_seqs, max_blocks_per_seq]                  int32
+ *                entries past ceil(seq_len / block_size) are never read
+ *   seq_lens     [num_seqs]                                      int32
+ *   out          [num_seqs, num_heads, head_dim]                 dtype
+ *   tmp_output   [num_seqs, num_heads, max_num_partitions, head_dim] float32
+ *   exp_sums     [num_seqs, num_heads, max_num_partitions]       float32
+ *   max_logits   [num_seqs, num_heads, max_num_partitions]       float32
+ *   dtype is PA_F16 (IEEE binary16) or PA_BF16 (bfloat16); arithmetic is
+ *   fp32 throughout; out is rounded to dtype to nearest-even.
+ *   Partition slots p >= ceil(seq_lens[b]/partition_size) are left untouched.
+ *   A sequence with seq_len 0 gets a zero output row.
+ *
+ * Supported shapes: head_dim == 128; block_size 16 or 32;
+ * partition_size a positive multiple of block_size; G = num_heads /
+ * num_kv_heads an integer in [1, 16].  Other shapes return
+ * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned
+ * (they are read with the Tensor Memory Accelerator); query and out 4-byte
+ * aligned.
+ *
+ * Ownership, synchronisation, errors
+ * ----------------------------------
+ * Every pointer is owned and allocated by the caller; the library never
+ * allocates, frees or synchronises.  Work is enqueued on `stream` (NULL is
+ * the legacy default stream) and is asynchronous.  Arguments are validated
+ * on the host before anything is enqueued: an invalid call returns a
+ * non-zero PA_ERR_* code and launches nothing.  A launch failure returns
+ * PA_ERR_CUDA.  Problems only the device can see are OR-ed as PA_STATUS_*
+ * bits into *status (a device int32 the caller zeroes; may be NULL):
+ *   PA_STATUS_BAD_BLOCK_ID  a needed block_tables entry is outside
+ *                           [0, num_blocks); that block is read from
+ *                           physical block 0 instead (the output is then
+ *                           meaningless but no memory outside the caches
+ *                           is touched);
+ *   PA_STATUS_BAD_SEQ_LEN   seq_lens[b] < 0 or > max_blocks_per_seq *
+ *                           block_size; the length is clamped into range;
+ *   PA_STATUS_TIMEOUT       a bounded wait for a shared-memory copy gave up
+ *                           (after about a second) instead of hanging.
+ * The caller reads *status after synchronising the stream.
+ * Entry points are thread-safe; the only global state is a per-device
+ * cache of the multiprocessor count and of the kernels' shared-memory
+ * opt-in.
+ */
+#ifndef PA_DECODE_H
+#define PA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_API __attribute__((visibility("default")))
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *pa_stream_t;
+
+enum { PA_F16 = 0, PA_BF16 = 1 };
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, inconsistent sizes */
+    PA_ERR_UNSUPPORTED = 2, /* valid but not implemented (head_dim, block_size, G) */
+    PA_ERR_WORKSPACE = 3,   /* max_num_partitions too small for the sequences */
+    PA_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+};
+
+enum {
+    PA_STATUS_BAD_BLOCK_ID = 1,
+    PA_STATUS_BAD_SEQ_LEN = 2,
+    PA_STATUS_TIMEOUT = 4
+};
+
+/*
+ * Number of partitions ceil(max_seq_len / partition_size) that phase 1 uses
+ * for the longest sequence ("vllm/_custom_ops.py" commit 900ae0b, change 1:
+ * 100K tokens / 1024 = 98 partitions).  Returns -1 for invalid arguments.
+ */
+PA_API int pa_v2_num_partitions(int max_seq_len, int partition_size);
+
+/*
+ * Bytes of the three phase-1 intermediates (tmp_output, exp_sums,
+ * max_logits) for the given capacity: num_seqs * num_heads *
+ * max_num_partitions * (head_dim + 2) * 4.  The caller allocates them once
+ * and reuses them ("paged_attn.py" commit 490ff98, change 2: pre-allocate
+ * the V2 intermediates).  Returns 0 for invalid arguments.
+ */
+PA_API size_t pa_v2_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                    int max_num_partitions);
+
+/*
+ * Two-pass split-K decode (phase 1 then phase 2 on `stream`), see above.
+ * max_seq_len_hint: if > 0, an upper bound of every seq_lens[b] known on the
+ *   host; phase 1 then launches ceil(hint / partition_size) partitions per
+ *   sequence.  If <= 0, ceil(max_blocks_per_seq * block_size /
+ *   partition_size) are launched and the unused ones exit at once.  A
+ *   sequence longer than the hint sets PA_STATUS_BAD_SEQ_LEN.
+ * max_num_partitions: the partition capacity (third dimension) of
+ *   tmp_output / exp_sums / max_logits; it must be >= the launched count,
+ *   else PA_ERR_WORKSPACE.
+ */
+PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                        int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                        int partition_size, int dtype, void *out, float *tmp_output,
+                        float *exp_sums, float *max_logits, int max_num_partitions,
+                        int32_t *status, pa_stream_t stream);
+
+/*
+ * Phase 1 alone: writes tmp_output, exp_sums and max_logits for every
+ * partition (same arguments as pa_decode_v2 without `out`).
+ */
+PA_API int pa_decode_v2_phase1(const void *query, const void *key_cache, const void *value_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                               int block_size, int max_blocks_per_seq, int max_seq_len_hint,
+                               float scale, int partition_size, int dtype, float *tmp_output,
+                               float *exp_sums, float *max_logits, int max_num_partitions,
+                               int32_t *status, pa_stream_t stream);
+
+/*
+ * Phase 2 alone: the log-sum-exp merge of the partitions phase 1 wrote
+ * (reads ceil(seq_lens[b] / partition_size) partitions of each (b, h)).
+ */
+PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_heads,
+                               int head_dim, int max_seq_len, int partition_size, int dtype,
+                               const float *tmp_output, const float *exp_sums,
+                               const float *max_logits, int max_num_partitions, void *out,
+                               int32_t *status, pa_stream_t stream);
+
+/*
+ * Single-pass decode: one CTA per (sequence, KV head) walks all blocks with
+ * a running {m, l, o} and writes `out` directly.  No intermediates.
+ */
+PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                        int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                        int dtype, void *out, int32_t *status, pa_stream_t stream);
+
+/*
+ * Which variant pa_decode runs for these sizes on the current device:
+ * returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.  Host only.
+ */
+PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size);
+
+/*
+ * V1/V2 dispatch: runs pa_decode_v1 or pa_decode_v2 as pa_decode_choose
+ * says for (num_seqs, num_kv_heads, L, partition_size), where L is
+ * max_seq_len_hint if > 0, else max_blocks_per_seq * block_size.  The V2
+ * intermediates must be valid whenever V2 can be chosen.
+ */
+PA_API int pa_decode(const void *query, const void *key_cache, const void *value_cache,
+                     const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                     int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                     int partition_size, int dtype, void *out, float *tmp_output,
+                     float *exp_sums, float *max_logits, int max_num_partitions,
+                     int32_t *status, pa_stream_t stream);
+
+/*
+ * Launch-shape override for the attention kernels, process-wide: warps per
+ * CTA (1..8) and TMA ring stages per warp (1..8); 0 keeps the built-in
+ * choice for that field.  The override never changes results, only speed.
+ * Returns PA_ERR_INVALID_ARG for out-of-range values.
+ */
+PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
+
+/* Human-readable name of a PA_* return code (static string). */
+PA_API const char *pa_status_string(int code);
+
+/*
+ * Self-test of the bounded-wait path used by every kernel above: launches
+ * one warp that waits on a shared-memory barrier nothing ever completes,
+ * for at most limit_ns nanoseconds, then ORs PA_STATUS_TIMEOUT into
+ * *status and returns.  Shows that a stuck copy turns into an error status
+ * instead of a hung GPU.  limit_ns must be in (0, 2e9].
+ */
+PA_API int pa_selftest_wait_timeout(int32_t *status, long long limit_ns, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_DECODE_H */

@@ -1,0 +1,460 @@
+// pa_api.cu -- the C ABI declared in include/pa_decode.h: host-side
+// validation, TMA descriptor encoding, launch sizing, V1/V2 dispatch.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "pa_decode.h"
+#include "pa_internal.h"
+
+using namespace pa;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kMaxSmem = 227 * 1024;
+
+std::atomic<int> g_tune_warps{0};
+std::atomic<int> g_tune_stages{0};
+
+// Per-device cached multiprocessor count (0 = not queried yet).
+std::atomic<int> g_sm_count[kMaxDevices];
+// Per-device, per-kernel dynamic shared memory already opted into.
+std::atomic<int> g_smem_optin[kMaxDevices][16];
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+int current_device(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices)
+        return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+int sm_count(int dev)
+{
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return -1;
+        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by every attention entry point.  No CUDA call.
+int check_shape(const void *query, const void *key_cache, const void *value_cache,
+                const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+                int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                int max_blocks_per_seq, float scale, int dtype)
+{
+    if (!query || !key_cache || !value_cache || !block_tables || !seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 ||
+        block_size <= 0 || max_blocks_per_seq <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (num_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim)
+        return PA_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32)
+        return PA_ERR_UNSUPPORTED;
+    if (num_heads / num_kv_heads > kMaxGroup)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_kv_heads > 65535)
+        return PA_ERR_UNSUPPORTED;
+    // TMA row coordinates and token indices are 32-bit.
+    if ((int64_t)num_blocks * num_kv_heads * block_size > INT32_MAX ||
+        (int64_t)max_blocks_per_seq * block_size > INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(query, 4))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+int seq_cap(int max_blocks_per_seq, int block_size, int hint)
+{
+    const int full = max_blocks_per_seq * block_size;
+    return (hint > 0 && hint < full) ? hint : full;
+}
+
+// 3-D view of a cache for the TMA: dims {64 (inner half of head_dim), 2 (halves),
+// rows = num_blocks * KV * block_size}, 128-byte swizzle, box {64, 1, block_size}.
+int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
+                     int num_kv_heads, int block_size)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+    if (!fn)
+        return PA_ERR_CUDA;
+    const cuuint64_t rows = (cuuint64_t)num_blocks * num_kv_heads * block_size;
+    const cuuint64_t dims[3] = {64, 2, rows};
+    const cuuint64_t strides[2] = {128, 256}; // bytes of dim 1 and dim 2
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)block_size};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = fn(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+int kernel_slot(int dtype, int block_size, int group, bool v1)
+{
+    return (dtype == PA_BF16 ? 8 : 0) | (block_size == 32 ? 4 : 0) | (group > 8 ? 2 : 0) | (v1 ? 1 : 0);
+}
+
+// Picks warps / stages / shared memory for the attention kernel.
+void size_attn(AttnLaunch &L)
+{
+    int warps = g_tune_warps.load(std::memory_order_relaxed);
+    int stages = g_tune_stages.load(std::memory_order_relaxed);
+    if (warps <= 0)
+        warps = 4;
+    if (stages <= 0)
+        stages = L.block_size == 16 ? 3 : 2;
+    const size_t sb = stage_bytes(L.block_size);
+    while ((size_t)stages * sb < warp_scratch_bytes(L.p.group))
+        ++stages;
+    while (1024 + (size_t)warps * stages * sb > kMaxSmem && stages > 1)
+        --stages;
+    while (1024 + (size_t)warps * stages * sb > kMaxSmem && warps > 1)
+        --warps;
+    L.warps = warps;
+    L.p.stages = stages;
+    L.smem_bytes = 1024 + (size_t)warps * stages * sb;
+}
+
+int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
+{
+    int dev;
+    if (current_device(&dev))
+        return PA_ERR_CUDA;
+    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
+    if (g_smem_optin[dev][slot].load(std::memory_order_relaxed) < (int)L.smem_bytes) {
+        cudaError_t e = L.dtype == PA_BF16
+                            ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, L.smem_bytes)
+                            : attn_prepare_f16(L.block_size, L.p.group, L.v1, L.smem_bytes);
+        if (e != cudaSuccess)
+            return PA_ERR_CUDA;
+        g_smem_optin[dev][slot].store((int)L.smem_bytes, std::memory_order_relaxed);
+    }
+    cudaError_t e = L.dtype == PA_BF16 ? launch_attn_bf16(L, stream) : launch_attn_f16(L, stream);
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+// Builds the attention launch (V2 phase 1 or V1) after validation.
+int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+               int num_kv_heads, int num_blocks, int block_size, int max_blocks_per_seq, int cap,
+               float scale, int dtype, bool v1, int num_partitions, int partition_size,
+               float *tmp_output, float *exp_sums, float *max_logits, int max_num_partitions,
+               void *out, int32_t *status)
+{
+    std::memset(&L, 0, sizeof(L));
+    int rc = encode_cache_map(&L.tmap_k, key_cache, dtype, num_blocks, num_kv_heads, block_size);
+    if (rc)
+        return rc;
+    rc = encode_cache_map(&L.tmap_v, value_cache, dtype, num_blocks, num_kv_heads, block_size);
+    if (rc)
+        return rc;
+    AttnParams &p = L.p;
+    p.query = query;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.num_heads = num_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_heads / num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.seq_len_cap = cap;
+    p.scale = scale;
+    p.part_blocks = v1 ? 0 : partition_size / block_size;
+    p.max_num_partitions = max_num_partitions;
+    p.tmp_output = tmp_output;
+    p.exp_sums = exp_sums;
+    p.max_logits = max_logits;
+    p.out = out;
+    p.status = status;
+    L.block_size = block_size;
+    L.dtype = dtype;
+    L.v1 = v1;
+    L.grid = dim3(v1 ? 1 : num_partitions, num_kv_heads, num_seqs);
+    size_attn(L);
+    return PA_OK;
+}
+
+int v2_phase1_impl(const void *query, const void *key_cache, const void *value_cache,
+                   const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                   int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                   int max_blocks_per_seq, int max_seq_len_hint, float scale, int partition_size,
+                   int dtype, float *tmp_output, float *exp_sums, float *max_logits,
+                   int max_num_partitions, int32_t *status, cudaStream_t stream, int *cap_out)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    if (partition_size <= 0 || partition_size % block_size != 0)
+        return PA_ERR_INVALID_ARG;
+    if (!tmp_output || !exp_sums || !max_logits || max_num_partitions <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(tmp_output, 16) || !aligned(exp_sums, 4) || !aligned(max_logits, 4))
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    const int np = pa_v2_num_partitions(cap, partition_size);
+    if (np > max_num_partitions)
+        return PA_ERR_WORKSPACE;
+    if (cap_out)
+        *cap_out = cap;
+    if (np == 0)
+        return PA_OK;
+    AttnLaunch L;
+    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
+                    num_kv_heads, num_blocks, block_size, max_blocks_per_seq, cap, scale, dtype,
+                    false, np, partition_size, tmp_output, exp_sums, max_logits,
+                    max_num_partitions, nullptr, status);
+    if (rc)
+        return rc;
+    return prepare_and_launch_attn(L, stream);
+}
+
+int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int head_dim,
+                   int max_seq_len, int partition_size, int dtype, const float *tmp_output,
+                   const float *exp_sums, const float *max_logits, int max_num_partitions,
+                   void *out, int32_t *status, cudaStream_t stream)
+{
+    if (!seq_lens || !tmp_output || !exp_sums || !max_logits || !out)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_seq_len < 0 ||
+        partition_size <= 0 || max_num_partitions <= 0)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F16 && dtype != PA_BF16)
+        return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDim)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs > 65535 || num_heads > INT32_MAX / 2)
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned(tmp_output, 16) || !aligned(out, 2))
+        return PA_ERR_INVALID_ARG;
+    if (pa_v2_num_partitions(max_seq_len, partition_size) > max_num_partitions)
+        return PA_ERR_WORKSPACE;
+    MergeParams p;
+    p.seq_lens = seq_lens;
+    p.num_heads = num_heads;
+    p.seq_len_cap = max_seq_len;
+    p.partition_size = partition_size;
+    p.max_num_partitions = max_num_partitions;
+    p.tmp_output = tmp_output;
+    p.exp_sums = exp_sums;
+    p.max_logits = max_logits;
+    p.out = out;
+    p.status = status;
+    return launch_merge(dtype, p, num_seqs, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size, int sms)
+{
+    const int np = pa_v2_num_partitions(max_seq_len, partition_size);
+    if (np <= 1)
+        return 1; // one partition: the merge pass would only copy
+    // V1 runs one CTA per (seq, KV head).  Prefer it only when those CTAs
+    // alone already cover the GPU several times over and each walks at most a
+    // few partitions' worth of blocks; otherwise split the sequence (V2).
+    const long long ctas = (long long)num_seqs * num_kv_heads;
+    if (ctas >= 4LL * sms && np <= 4)
+        return 1;
+    return 2;
+}
+
+} // namespace
+
+extern "C" {
+
+PA_API int pa_v2_num_partitions(int max_seq_len, int partition_size)
+{
+    if (max_seq_len < 0 || partition_size <= 0)
+        return -1;
+    return (int)(((long long)max_seq_len + partition_size - 1) / partition_size);
+}
+
+PA_API size_t pa_v2_workspace_bytes(int num_seqs, int num_heads, int head_dim,
+                                    int max_num_partitions)
+{
+    if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_num_partitions <= 0)
+        return 0;
+    return (size_t)num_seqs * num_heads * max_num_partitions * (size_t)(head_dim + 2) * 4;
+}
+
+PA_API int pa_decode_v2_phase1(const void *query, const void *key_cache, const void *value_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                               int block_size, int max_blocks_per_seq, int max_seq_len_hint,
+                               float scale, int partition_size, int dtype, float *tmp_output,
+                               float *exp_sums, float *max_logits, int max_num_partitions,
+                               int32_t *status, pa_stream_t stream)
+{
+    return v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                          num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                          max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
+                          tmp_output, exp_sums, max_logits, max_num_partitions, status,
+                          (cudaStream_t)stream, nullptr);
+}
+
+PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_heads,
+                               int head_dim, int max_seq_len, int partition_size, int dtype,
+                               const float *tmp_output, const float *exp_sums,
+                               const float *max_logits, int max_num_partitions, void *out,
+                               int32_t *status, pa_stream_t stream)
+{
+    return v2_phase2_impl(seq_lens, num_seqs, num_heads, head_dim, max_seq_len, partition_size,
+                          dtype, tmp_output, exp_sums, max_logits, max_num_partitions, out,
+                          status, (cudaStream_t)stream);
+}
+
+PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                        int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                        int partition_size, int dtype, void *out, float *tmp_output,
+                        float *exp_sums, float *max_logits, int max_num_partitions,
+                        int32_t *status, pa_stream_t stream)
+{
+    if (!out || !aligned(out, 2))
+        return PA_ERR_INVALID_ARG;
+    int cap = 0;
+    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
+                            tmp_output, exp_sums, max_logits, max_num_partitions, status,
+                            (cudaStream_t)stream, &cap);
+    if (rc)
+        return rc;
+    return v2_phase2_impl(seq_lens, num_seqs, num_heads, head_dim, cap, partition_size, dtype,
+                          tmp_output, exp_sums, max_logits, max_num_partitions, out, status,
+                          (cudaStream_t)stream);
+}
+
+PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                        int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                        int dtype, void *out, int32_t *status, pa_stream_t stream)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    if (!out || !aligned(out, 2))
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    AttnLaunch L;
+    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
+                    num_kv_heads, num_blocks, block_size, max_blocks_per_seq, cap, scale, dtype,
+                    true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
+    if (rc)
+        return rc;
+    return prepare_and_launch_attn(L, (cudaStream_t)stream);
+}
+
+PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size)
+{
+    if (num_seqs <= 0 || num_kv_heads <= 0 || max_seq_len < 0 || partition_size <= 0)
+        return -PA_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(&dev))
+        return -PA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return -PA_ERR_CUDA;
+    return choose_variant(num_seqs, num_kv_heads, max_seq_len, partition_size, sms);
+}
+
+PA_API int pa_decode(const void *query, const void *key_cache, const void *value_cache,
+                     const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                     int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
+                     int partition_size, int dtype, void *out, float *tmp_output,
+                     float *exp_sums, float *max_logits, int max_num_partitions,
+                     int32_t *status, pa_stream_t stream)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    if (partition_size <= 0 || partition_size % block_size != 0)
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    const int which = pa_decode_choose(num_seqs, num_kv_heads, cap, partition_size);
+    if (which < 0)
+        return -which;
+    if (which == 1)
+        return pa_decode_v1(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                            max_blocks_per_seq, max_seq_len_hint, scale, dtype, out, status,
+                            stream);
+    return pa_decode_v2(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                        num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                        max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype, out,
+                        tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
+}
+
+PA_API const char *pa_status_string(int code)
+{
+    switch (code) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    default: return "PA_UNKNOWN";
+    }
+}
+
+PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp)
+{
+    if (warps_per_cta < 0 || warps_per_cta > kMaxWarps || stages_per_warp < 0 ||
+        stages_per_warp > kMaxStages)
+        return PA_ERR_INVALID_ARG;
+    g_tune_warps.store(warps_per_cta, std::memory_order_relaxed);
+    g_tune_stages.store(stages_per_warp, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+PA_API int pa_selftest_wait_timeout(int32_t *status, long long limit_ns, pa_stream_t stream)
+{
+    if (!status || limit_ns <= 0 || limit_ns > 2000000000LL)
+        return PA_ERR_INVALID_ARG;
+    return launch_wait_selftest(status, (unsigned long long)limit_ns, (cudaStream_t)stream) ==
+                   cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+} // extern "C"

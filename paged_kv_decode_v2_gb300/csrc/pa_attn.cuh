@@ -1,0 +1,450 @@
+// pa_attn.cuh -- the attention kernel: phase 1 of split-K decode ("V2") and
+// the single-pass form ("V1").
+//
+// One CTA owns one (partition p, KV head k, sequence b) -- for V1 the
+// "partition" is the whole sequence.  It serves the whole GQA group of G
+// query heads that share KV head k, so every K/V byte is read from HBM once
+// per call ("paged_attention_v2_pytorch.py" commit 15ef28e, "Key changes":
+// GQA by broadcasting the KV head instead of replicating it).
+//
+// Data movement.  Each warp of the CTA owns a private ring of `stages`
+// shared-memory stages and walks the blocks j = warp, warp + W, ... of the
+// CTA's range.  A stage holds one paged block's K tile and V tile
+// (block_size rows x 128 dims each), brought in by four TMA tensor loads
+// (K and V, two 64-dim halves) that complete on the stage's mbarrier.  The
+// block id is read from the block table a full chunk of 32 blocks ahead of
+// use.  Loads use 128-byte swizzling, so the ldmatrix reads below touch 32
+// distinct banks.
+//
+// Math (fp32 accumulation on the tensor cores, mma.sync m16n8k16).  Tokens
+// are the M dimension and query heads the N dimension (8 per n-tile), so a
+// GQA group of 8 fills an n-tile exactly:
+//     S^T[16 tokens x 8 heads]  = K_tile[16 x 128] . Q^T[128 x 8]   (8 MMAs)
+//     O^T[128 x 8 heads]       += V_tile^T[128 x 16] . P^T[16 x 8]  (8 MMAs)
+// Q^T lives in registers for the whole CTA.  The S^T accumulator fragment is
+// turned into the P^T operand fragment with two movmatrix transposes.  The
+// softmax is the streaming {m, l, o} accumulator with the merge factor
+// exp(m_old - m_new) ("paged_attn.py" commit 490ff98, the
+// summary_statistics paragraph), kept per warp and merged across warps at
+// the end with the same rule.
+//
+// Output.  V2 writes, per query head of the group, the partition's
+//     max_logits = m_p,  exp_sums = l_p = sum exp(s - m_p),
+//     tmp_output = sum exp(s - m_p) V / l_p
+// ("paged_attention_v2_pytorch.py" commit 9cb7f9d, "Implementation",
+// Phase 1).  V1 writes out = o / l rounded to the storage type.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename T, int BS, int NT, bool V1>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
+{
+    using E = Elem<T>;
+    constexpr uint32_t kHalfBytes = BS * 128;      // one 64-dim half of a tile
+    constexpr uint32_t kStageBytes = 4 * kHalfBytes; // K0 K1 V0 V1
+    constexpr int kTiles = BS / 16;                  // 16-row MMA tiles per block
+    constexpr int kHeads = NT * 8;
+
+    __shared__ uint64_t bars[kMaxWarps * kMaxStages];
+    __shared__ float s_factor[kMaxWarps][kMaxGroup];
+    __shared__ float s_stat[2][kMaxGroup]; // merged max, merged sum
+    extern __shared__ uint8_t dyn_smem[];
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int g4 = lane >> 2; // row group of the mma fragments
+    const int t4 = lane & 3;  // thread within the group
+
+    const int part = blockIdx.x;
+    const int kv = blockIdx.y;
+    const int b = blockIdx.z;
+
+    // ---- sequence range owned by this CTA
+    int L = __ldg(&p.seq_lens[b]);
+    if (L < 0 || L > p.seq_len_cap) {
+        if (threadIdx.x == 0 && part == 0 && kv == 0)
+            set_status(p.status, PA_STATUS_BAD_SEQ_LEN);
+        L = L < 0 ? 0 : p.seq_len_cap;
+    }
+    int tok0 = 0, ntok = L;
+    if (!V1) {
+        tok0 = part * p.part_blocks * BS;
+        if (tok0 >= L)
+            return; // partition past the end of this sequence: nothing to write
+        ntok = min(p.part_blocks * BS, L - tok0);
+    }
+    const int nblk = (ntok + BS - 1) / BS;
+    const int blk0 = tok0 / BS;
+    const int head0 = kv * p.group;
+
+    if (V1 && nblk == 0) { // empty sequence: zero output
+        T *out = static_cast<T *>(p.out);
+        for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += blockDim.x)
+            out[((size_t)b * p.num_heads + head0) * kHeadDim + idx] = E::from_float(0.f);
+        return;
+    }
+
+    const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+    const uint32_t ring = smem0 + (uint32_t)warp * (uint32_t)p.stages * kStageBytes;
+    const uint32_t bar0 = smem_addr(&bars[warp * kMaxStages]);
+    const int stages = p.stages;
+
+    // Blocks of this warp: j = warp + nwarps * i, i < cnt.
+    const int cnt = warp < nblk ? (nblk - warp + nwarps - 1) / nwarps : 0;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
+
+    if (lane == 0) {
+        for (int s = 0; s < stages; ++s)
+            mbar_init(bar0 + 8 * s, 1);
+        mbar_init_fence();
+        if (warp == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+    }
+    __syncwarp();
+
+    const uint64_t policy = l2_evict_first_policy();
+    int32_t status_bits = 0;
+
+    // Block ids, a chunk of 32 per warp, with the next chunk in flight.
+    auto load_ids = [&](int chunk) -> int32_t {
+        const int i = chunk * 32 + lane;
+        return i < cnt ? __ldg(bt_row + (size_t)nwarps * i) : 0;
+    };
+    int32_t ids_cur = load_ids(0);
+    int32_t ids_next = load_ids(1);
+    int chunk_cur = 0;
+
+    // Issue the four TMA loads of the warp's i-th block into stage s (warp-uniform call).
+    auto issue = [&](int i, int s) {
+        const int c = i >> 5;
+        if (c != chunk_cur) {
+            ids_cur = ids_next;
+            ids_next = load_ids(c + 1);
+            chunk_cur = c;
+        }
+        int32_t phys = __shfl_sync(0xffffffffu, ids_cur, i & 31);
+        if (phys < 0 || phys >= p.num_blocks) {
+            status_bits |= PA_STATUS_BAD_BLOCK_ID;
+            phys = 0; // read a valid block instead of memory outside the cache
+        }
+        if (lane == 0) {
+            const uint32_t bar = bar0 + 8 * s;
+            const uint32_t dst = ring + (uint32_t)s * kStageBytes;
+            const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
+            mbar_arrive_expect_tx(bar, kStageBytes);
+            tma_load_3d(dst, &tmap_k, 0, 0, row, bar, policy);
+            tma_load_3d(dst + kHalfBytes, &tmap_k, 0, 1, row, bar, policy);
+            tma_load_3d(dst + 2 * kHalfBytes, &tmap_v, 0, 0, row, bar, policy);
+            tma_load_3d(dst + 3 * kHalfBytes, &tmap_v, 0, 1, row, bar, policy);
+        }
+    };
+
+    int issued = 0;
+    for (; issued < cnt && issued < stages; ++issued)
+        issue(issued, issued);
+
+    // ---- Q^T fragments (B operand of S^T = K Q^T): head 8j + g4, dims 16ks + 2t4 (+1, +8, +9)
+    uint32_t qf[NT][8][2];
+    {
+        const uint32_t *q32 = static_cast<const uint32_t *>(p.query);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int g = j * 8 + g4;
+            const bool has = g < p.group;
+            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (kHeadDim / 2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qf[j][ks][0] = has ? __ldg(q32 + rowbase + ks * 8 + t4) : 0u;
+                qf[j][ks][1] = has ? __ldg(q32 + rowbase + ks * 8 + 4 + t4) : 0u;
+            }
+        }
+    }
+
+    // Running softmax state of this lane's heads 8j + 2t4 (+1): natural-log units.
+    float m_run[NT][2], l_run[NT][2];
+    float o[NT][8][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        m_run[j][0] = m_run[j][1] = -INFINITY;
+        l_run[j][0] = l_run[j][1] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+            o[j][mt][0] = o[j][mt][1] = o[j][mt][2] = o[j][mt][3] = 0.f;
+    }
+
+    // Per-lane ldmatrix row offsets.  ldmatrix lane L addresses row (L & 7) of 8x8 matrix L >> 3.
+    const int mrow = lane & 7;
+    const int mq = lane >> 3;
+    // K (non-transposed A operand): matrix q covers rows (q & 1) * 8 .., dims (q >> 1) * 8 ..
+    const int k_row = (mq & 1) * 8 + mrow;
+    const int k_chunk_hi = mq >> 1;
+    // V (transposed A operand): matrix q covers dims (q & 1) * 8 .., tokens (q >> 1) * 8 ..
+    const int v_row = (mq >> 1) * 8 + mrow;
+    const int v_chunk_lo = mq & 1;
+
+    const float scale = p.scale;
+    int i = 0;
+    for (; i < cnt; ++i) {
+        const int s = i % stages;
+        const uint32_t parity = (uint32_t)(i / stages) & 1u;
+        if (!mbar_wait_bounded(bar0 + 8 * s, parity, kWaitLimitNs)) {
+            status_bits |= PA_STATUS_TIMEOUT;
+            break;
+        }
+        const int jblk = warp + nwarps * i;
+        const int valid = min(BS, ntok - jblk * BS);
+        const uint32_t kbase = ring + (uint32_t)s * kStageBytes;
+        const uint32_t vbase = kbase + 2 * kHalfBytes;
+
+        if (valid < BS) {
+            // Rows past the end of the sequence: zero V so no stale value reaches P.V.
+            const int nchunks = (BS - valid) * 16;
+            for (int c = lane; c < nchunks; c += 32) {
+                const int r = valid + (c >> 4);
+                const int h = (c >> 3) & 1;
+                st_shared_zero16(vbase + h * kHalfBytes + r * 128 + (c & 7) * 16);
+            }
+            __syncwarp();
+        }
+
+#pragma unroll
+        for (int tile = 0; tile < kTiles; ++tile) {
+            if (tile * 16 >= valid)
+                break;
+            // ---- S^T = K_tile Q^T
+            uint32_t ka[8][4];
+            {
+                const int r = tile * 16 + k_row;
+                const uint32_t rbase = kbase + r * 128;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int chunk = ((ks & 3) << 1) | k_chunk_hi;
+                    ldsm_x4(rbase + (ks >> 2) * kHalfBytes + ((chunk ^ mrow) << 4), ka[ks]);
+                }
+            }
+            float sacc[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float e[4] = {0.f, 0.f, 0.f, 0.f};
+                float f[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 8; ks += 2) {
+                    E::mma(e, ka[ks], qf[j][ks][0], qf[j][ks][1]);
+                    E::mma(f, ka[ks + 1], qf[j][ks + 1][0], qf[j][ks + 1][1]);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    sacc[j][c] = e[c] + f[c];
+            }
+
+            // ---- scale, mask, streaming softmax update
+            const int r0 = tile * 16 + g4; // token rows of c0/c1 and (r0 + 8) of c2/c3
+            const bool ok0 = r0 < valid;
+            const bool ok1 = r0 + 8 < valid;
+            uint32_t pb[NT][2][2]; // [n-tile][hi/lo][b0/b1]
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                float sv[4];
+                sv[0] = ok0 ? sacc[j][0] * scale : -INFINITY;
+                sv[1] = ok0 ? sacc[j][1] * scale : -INFINITY;
+                sv[2] = ok1 ? sacc[j][2] * scale : -INFINITY;
+                sv[3] = ok1 ? sacc[j][3] * scale : -INFINITY;
+                float mx0 = fmaxf(sv[0], sv[2]);
+                float mx1 = fmaxf(sv[1], sv[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m_run[j][0], mx0);
+                const float mn1 = fmaxf(m_run[j][1], mx1);
+                const float a0 = fast_exp2((m_run[j][0] - mn0) * kLog2e);
+                const float a1 = fast_exp2((m_run[j][1] - mn1) * kLog2e);
+                m_run[j][0] = mn0;
+                m_run[j][1] = mn1;
+                const float mb0 = mn0 * kLog2e, mb1 = mn1 * kLog2e;
+                float pv[4];
+                pv[0] = fast_exp2(fmaf(sv[0], kLog2e, -mb0));
+                pv[1] = fast_exp2(fmaf(sv[1], kLog2e, -mb1));
+                pv[2] = fast_exp2(fmaf(sv[2], kLog2e, -mb0));
+                pv[3] = fast_exp2(fmaf(sv[3], kLog2e, -mb1));
+                l_run[j][0] = fmaf(l_run[j][0], a0, pv[0] + pv[2]);
+                l_run[j][1] = fmaf(l_run[j][1], a1, pv[1] + pv[3]);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[j][mt][0] *= a0;
+                    o[j][mt][1] *= a1;
+                    o[j][mt][2] *= a0;
+                    o[j][mt][3] *= a1;
+                }
+                // P^T fragments: pack (token row, head pair) and transpose to (token pair, head).
+                const uint32_t h01 = E::pack(pv[0], pv[1]);
+                const uint32_t h23 = E::pack(pv[2], pv[3]);
+                pb[j][0][0] = movmatrix_trans(h01);
+                pb[j][0][1] = movmatrix_trans(h23);
+                if (E::kSplitP) {
+                    const uint32_t l01 = E::pack(pv[0] - E::lo(h01), pv[1] - E::hi(h01));
+                    const uint32_t l23 = E::pack(pv[2] - E::lo(h23), pv[3] - E::hi(h23));
+                    pb[j][1][0] = movmatrix_trans(l01);
+                    pb[j][1][1] = movmatrix_trans(l23);
+                }
+            }
+
+            // ---- O^T += V_tile^T P^T
+            {
+                const int r = tile * 16 + v_row;
+                const uint32_t rbase = vbase + r * 128;
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    uint32_t va[4];
+                    const int chunk = ((mt & 3) << 1) | v_chunk_lo;
+                    ldsm_x4_trans(rbase + (mt >> 2) * kHalfBytes + ((chunk ^ mrow) << 4), va);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        E::mma(o[j][mt], va, pb[j][0][0], pb[j][0][1]);
+                        if (E::kSplitP)
+                            E::mma(o[j][mt], va, pb[j][1][0], pb[j][1][1]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (issued < cnt) {
+            if (valid < BS)
+                fence_proxy_async();
+            issue(issued, s);
+            ++issued;
+        }
+    }
+
+    if (status_bits & PA_STATUS_TIMEOUT) {
+        // Let copies still in flight into this warp's ring land before the
+        // shared memory is reused or released (bounded again).
+        for (int k = i; k < issued; ++k)
+            mbar_wait_bounded(bar0 + 8 * (k % stages), (uint32_t)(k / stages) & 1u, kWaitLimitNs);
+    }
+    if (status_bits && lane == 0)
+        set_status(p.status, status_bits);
+
+    // ---- hand the warp's {m, l, o} to the CTA merge (scratch = this warp's own ring)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l_run[j][0] += __shfl_xor_sync(0xffffffffu, l_run[j][0], off);
+            l_run[j][1] += __shfl_xor_sync(0xffffffffu, l_run[j][1], off);
+        }
+    }
+    float *scr = reinterpret_cast<float *>(dyn_smem + (ring - smem_addr(dyn_smem)));
+    float *scr_m = scr;
+    float *scr_l = scr + kHeads;
+    float *scr_o = scr + 2 * kHeads; // [kHeads][132]
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        const int hA = j * 8 + 2 * t4;
+        if (g4 == 0) {
+            scr_m[hA] = m_run[j][0];
+            scr_m[hA + 1] = m_run[j][1];
+            scr_l[hA] = l_run[j][0];
+            scr_l[hA + 1] = l_run[j][1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int d = mt * 16 + g4;
+            scr_o[hA * 132 + d] = o[j][mt][0];
+            scr_o[(hA + 1) * 132 + d] = o[j][mt][1];
+            scr_o[hA * 132 + d + 8] = o[j][mt][2];
+            scr_o[(hA + 1) * 132 + d + 8] = o[j][mt][3];
+        }
+    }
+    __syncthreads();
+
+    // ---- merge the warps: M = max m_w, f_w = exp(m_w - M), l = sum f_w l_w, o = sum f_w o_w / l
+    const uint32_t warp_stride = (uint32_t)stages * kStageBytes / 4; // floats between warp scratches
+    const float *scr0 = reinterpret_cast<const float *>(dyn_smem + (smem0 - smem_addr(dyn_smem)));
+    if (threadIdx.x < p.group) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int w = 0; w < nwarps; ++w)
+            M = fmaxf(M, scr0[w * warp_stride + h]);
+        float lsum = 0.f;
+        for (int w = 0; w < nwarps; ++w) {
+            const float mw = scr0[w * warp_stride + h];
+            const float f = mw == -INFINITY ? 0.f : fast_exp2((mw - M) * kLog2e);
+            s_factor[w][h] = f;
+            lsum = fmaf(f, scr0[w * warp_stride + kHeads + h], lsum);
+        }
+        s_stat[0][h] = M;
+        s_stat[1][h] = lsum;
+    }
+    __syncthreads();
+
+    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += blockDim.x) {
+        const int h = idx >> 7;
+        const int d = idx & 127;
+        float acc = 0.f;
+        for (int w = 0; w < nwarps; ++w)
+            acc = fmaf(s_factor[w][h], scr0[w * warp_stride + 2 * kHeads + h * 132 + d], acc);
+        const float lsum = s_stat[1][h];
+        const float val = acc / lsum;
+        const size_t bh = (size_t)b * p.num_heads + head0 + h;
+        if (V1) {
+            static_cast<T *>(p.out)[bh * kHeadDim + d] = E::from_float(val);
+        } else {
+            const size_t slot = bh * p.max_num_partitions + part;
+            p.tmp_output[slot * kHeadDim + d] = val;
+            if (d == 0) {
+                p.exp_sums[slot] = lsum;
+                p.max_logits[slot] = s_stat[0][h];
+            }
+        }
+    }
+}
+
+// Kernel dispatch on block size, n-tiles (G <= 8 or <= 16) and V1/V2.
+template <typename T>
+static const void *attn_kernel_ptr(int block_size, int group, bool v1)
+{
+    const bool nt2 = group > 8;
+#define PA_PICK(BS, NT)                                                                           \
+    return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, BS, NT, true>)                    \
+              : reinterpret_cast<const void *>(&attn_kernel<T, BS, NT, false>)
+    if (block_size == 16) {
+        if (nt2) {
+            PA_PICK(16, 2);
+        }
+        PA_PICK(16, 1);
+    }
+    if (nt2) {
+        PA_PICK(32, 2);
+    }
+    PA_PICK(32, 1);
+#undef PA_PICK
+}
+
+template <typename T>
+static cudaError_t attn_prepare(int block_size, int group, bool v1, size_t smem_bytes)
+{
+    return cudaFuncSetAttribute(attn_kernel_ptr<T>(block_size, group, v1),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+}
+
+template <typename T>
+static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
+{
+    const void *fn = attn_kernel_ptr<T>(L.block_size, L.p.group, L.v1);
+    void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
+                    const_cast<AttnParams *>(&L.p)};
+    return cudaLaunchKernel(fn, L.grid, dim3(L.warps * 32), args, L.smem_bytes, stream);
+}
+
+} // namespace pa

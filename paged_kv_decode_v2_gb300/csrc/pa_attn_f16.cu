@@ -1,0 +1,16 @@
+// Attention kernels (V2 phase 1 and V1) instantiated for binary16 storage.
+#include "pa_attn.cuh"
+
+namespace pa {
+
+cudaError_t attn_prepare_f16(int block_size, int group, bool v1, size_t smem_bytes)
+{
+    return attn_prepare<__half>(block_size, group, v1, smem_bytes);
+}
+
+cudaError_t launch_attn_f16(const AttnLaunch &L, cudaStream_t stream)
+{
+    return attn_launch<__half>(L, stream);
+}
+
+} // namespace pa

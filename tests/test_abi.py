@@ -1,0 +1,125 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects invalid arguments on the host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "pa_decode.h")
+
+FAKE = 0x10000  # a 64 KiB-aligned address that is never dereferenced on these paths
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"PA_API\s+[\w\s\*]*?\b(pa_\w+)\s*\(", text)
+
+
+def test_header_declares_the_entry_points():
+    names = set(declared_functions())
+    for n in ("pa_decode_v2", "pa_decode_v1", "pa_decode", "pa_decode_v2_phase1",
+              "pa_decode_v2_phase2", "pa_v2_num_partitions", "pa_v2_workspace_bytes",
+              "pa_status_string", "pa_decode_choose", "pa_selftest_wait_timeout",
+              "pa_set_launch_config"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(cuda_lib):
+    lib = ctypes.CDLL(cuda_lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_num_partitions(cuda_lib):
+    assert cuda_lib.num_partitions(100000, 1024) == 98
+    assert cuda_lib.num_partitions(100000, 512) == 196
+    assert cuda_lib.num_partitions(1000, 512) == 2
+    assert cuda_lib.num_partitions(0, 512) == 0
+    assert cuda_lib.num_partitions(512, 512) == 1
+    assert cuda_lib.num_partitions(513, 512) == 2
+    assert cuda_lib.num_partitions(-1, 512) == -1
+    assert cuda_lib.num_partitions(10, 0) == -1
+
+
+def test_workspace_bytes(cuda_lib):
+    assert cuda_lib.workspace_bytes(1, 32, 128, 196) == 32 * 196 * 130 * 4
+    assert cuda_lib.workspace_bytes(0, 32, 128, 196) == 0
+
+
+def test_status_strings(cuda_lib):
+    assert cuda_lib.status_string(0) == "PA_OK"
+    assert cuda_lib.status_string(3) == "PA_ERR_WORKSPACE"
+    assert cuda_lib.status_string(99) == "PA_UNKNOWN"
+
+
+def _v2(lib, **kw):
+    a = dict(query=FAKE, key_cache=FAKE, value_cache=FAKE, block_tables=FAKE, seq_lens=FAKE,
+             num_seqs=1, num_heads=8, num_kv_heads=2, head_dim=128, num_blocks=128, block_size=16,
+             max_blocks=63, hint=0, scale=0.088, partition_size=512, dtype=0, out=FAKE, tmp=FAKE,
+             es=FAKE, ml=FAKE, max_np=2, status=None, stream=None)
+    a.update(kw)
+    return lib.pa_decode_v2(a["query"], a["key_cache"], a["value_cache"], a["block_tables"],
+                            a["seq_lens"], a["num_seqs"], a["num_heads"], a["num_kv_heads"],
+                            a["head_dim"], a["num_blocks"], a["block_size"], a["max_blocks"],
+                            a["hint"], a["scale"], a["partition_size"], a["dtype"], a["out"],
+                            a["tmp"], a["es"], a["ml"], a["max_np"], a["status"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(query=None), 1),
+    (dict(out=None), 1),
+    (dict(tmp=None), 1),
+    (dict(num_seqs=0), 1),
+    (dict(num_heads=6, num_kv_heads=4), 1),
+    (dict(dtype=2), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(head_dim=64), 2),
+    (dict(block_size=8), 2),
+    (dict(num_heads=64, num_kv_heads=2), 2),
+    (dict(partition_size=500), 1),
+    (dict(partition_size=0), 1),
+    (dict(key_cache=FAKE + 8), 1),
+    (dict(max_np=1), 3),
+    (dict(hint=600, max_np=1), 3),
+])
+def test_invalid_arguments_fail_before_launch(cuda_lib, kw, code):
+    assert _v2(cuda_lib.load(), **kw) == code
+
+
+def test_invalid_arguments_v1_and_dispatch(cuda_lib):
+    lib = cuda_lib.load()
+    args = [FAKE] * 5 + [1, 8, 2, 64, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_v1(*args, 0, FAKE, None, None) == 2
+    args = [FAKE] * 5 + [1, 8, 2, 128, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_v1(*args, 0, None, None, None) == 1
+    assert lib.pa_decode(*args, 500, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
+    assert lib.pa_decode_v2_phase2(FAKE, 1, 8, 128, 1000, 512, 0, FAKE, FAKE, FAKE, 1, FAKE,
+                                   None, None) == 3
+    assert lib.pa_decode_v2_phase2(None, 1, 8, 128, 1000, 512, 0, FAKE, FAKE, FAKE, 2, FAKE,
+                                   None, None) == 1
+
+
+def test_launch_config_override_validation(cuda_lib):
+    assert cuda_lib.load().pa_set_launch_config(9, 2) == 1
+    assert cuda_lib.load().pa_set_launch_config(4, 9) == 1
+    assert cuda_lib.load().pa_set_launch_config(0, 0) == 0
+
+
+def test_selftest_rejects_bad_limits(cuda_lib):
+    lib = cuda_lib.load()
+    assert lib.pa_selftest_wait_timeout(None, 1000, None) == 1
+    assert lib.pa_selftest_wait_timeout(FAKE, 0, None) == 1
+    assert lib.pa_selftest_wait_timeout(FAKE, 3_000_000_000, None) == 1
+
+
+def test_binding_refuses_cpu_tensors(cuda_lib):
+    import torch
+    import workloads as wl
+    inp = wl.make_inputs(wl.TINY)
+    out = torch.empty_like(inp.query)
+    with pytest.raises(ValueError):
+        cuda_lib.pa_decode_v1(inp.query, inp.key_cache, inp.value_cache, inp.block_tables,
+                              inp.seq_lens, 0.088, out)
