@@ -75,7 +75,8 @@
  * The caller reads *status after synchronising the stream.
  * Entry points are thread-safe; the only global state is a per-device
  * cache of the multiprocessor count and of the kernels' shared-memory
- * opt-in.
+ * opt-in, plus a small per-thread cache of encoded TMA descriptors keyed
+ * by cache address and shape.
  */
 #ifndef PA_DECODE_H
 #define PA_DECODE_H

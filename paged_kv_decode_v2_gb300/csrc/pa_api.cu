@@ -23,8 +23,6 @@ std::atomic<int> g_tune_stages{0};
 
 // Per-device cached multiprocessor count (0 = not queried yet).
 std::atomic<int> g_sm_count[kMaxDevices];
-// Per-device, per-kernel dynamic shared memory already opted into.
-std::atomic<int> g_smem_optin[kMaxDevices][16];
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
@@ -103,8 +101,8 @@ int seq_cap(int max_blocks_per_seq, int block_size, int hint)
 
 // 3-D view of a cache for the TMA: dims {64 (inner half of head_dim), 2 (halves),
 // rows = num_blocks * KV * block_size}, 128-byte swizzle, box {64, 1, block_size}.
-int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
-                     int num_kv_heads, int block_size)
+int encode_cache_map_uncached(CUtensorMap *map, const void *base, int dtype, int num_blocks,
+                              int num_kv_heads, int block_size)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn)
@@ -122,30 +120,133 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_bloc
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
 
+// Small per-thread cache of encoded descriptors: a decode loop calls with the
+// same caches every step, so encoding happens once per (cache, shape).
+struct MapCacheEntry {
+    CUtensorMap map;
+    const void *base;
+    int dtype, num_blocks, num_kv_heads, block_size;
+    bool valid;
+};
+constexpr int kMapCacheSize = 8;
+thread_local MapCacheEntry t_map_cache[kMapCacheSize];
+thread_local int t_map_next = 0;
+
+int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
+                     int num_kv_heads, int block_size)
+{
+    for (int i = 0; i < kMapCacheSize; ++i) {
+        const MapCacheEntry &e = t_map_cache[i];
+        if (e.valid && e.base == base && e.dtype == dtype && e.num_blocks == num_blocks &&
+            e.num_kv_heads == num_kv_heads && e.block_size == block_size) {
+            *map = e.map;
+            return PA_OK;
+        }
+    }
+    int rc = encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size);
+    if (rc)
+        return rc;
+    MapCacheEntry &e = t_map_cache[t_map_next];
+    t_map_next = (t_map_next + 1) % kMapCacheSize;
+    e.map = *map;
+    e.base = base;
+    e.dtype = dtype;
+    e.num_blocks = num_blocks;
+    e.num_kv_heads = num_kv_heads;
+    e.block_size = block_size;
+    e.valid = true;
+    return PA_OK;
+}
+
 int kernel_slot(int dtype, int block_size, int group, bool v1)
 {
     return (dtype == PA_BF16 ? 8 : 0) | (block_size == 32 ? 4 : 0) | (group > 8 ? 2 : 0) | (v1 ? 1 : 0);
 }
 
-// Picks warps / stages / shared memory for the attention kernel.
-void size_attn(AttnLaunch &L)
+// Per-device: kernel already opted in to the maximum dynamic shared memory.
+std::atomic<int> g_prepared[kMaxDevices][16];
+// Per-device resident CTAs per SM at two stages per warp, stored + 1 (0 = not queried).
+std::atomic<int> g_occ2[kMaxDevices][16][kMaxWarps + 1];
+
+int ensure_prepared(int dev, const AttnLaunch &L)
 {
-    int warps = g_tune_warps.load(std::memory_order_relaxed);
-    int stages = g_tune_stages.load(std::memory_order_relaxed);
-    if (warps <= 0)
-        warps = 4;
-    if (stages <= 0)
-        stages = L.block_size == 16 ? 3 : 2;
+    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
+    if (g_prepared[dev][slot].load(std::memory_order_acquire))
+        return PA_OK;
+    cudaError_t e = L.dtype == PA_BF16 ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, kMaxSmem)
+                                       : attn_prepare_f16(L.block_size, L.p.group, L.v1, kMaxSmem);
+    if (e != cudaSuccess)
+        return PA_ERR_CUDA;
+    g_prepared[dev][slot].store(1, std::memory_order_release);
+    return PA_OK;
+}
+
+size_t attn_smem(int block_size, int warps, int stages)
+{
+    return 1024 + (size_t)warps * stages * stage_bytes(block_size);
+}
+
+int occupancy(int dev, const AttnLaunch &L, int warps, int stages)
+{
+    const size_t smem = attn_smem(L.block_size, warps, stages);
+    if (smem > kMaxSmem)
+        return 0;
+    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
+    if (stages == 2) {
+        const int c = g_occ2[dev][slot][warps].load(std::memory_order_relaxed);
+        if (c)
+            return c - 1;
+    }
+    const int n = L.dtype == PA_BF16
+                      ? attn_occupancy_bf16(L.block_size, L.p.group, L.v1, warps, smem)
+                      : attn_occupancy_f16(L.block_size, L.p.group, L.v1, warps, smem);
+    if (stages == 2)
+        g_occ2[dev][slot][warps].store(n + 1, std::memory_order_relaxed);
+    return n;
+}
+
+// Launch shape of the attention kernel.  Each warp keeps two ring stages
+// (one block being computed, one landing): the sweep on GB300 showed that
+// more stages per warp only lose CTAs per SM.  Phase 1 uses 4 warps for
+// 16-token blocks and 2 for 32-token blocks (about 64 KB of shared memory,
+// three CTAs per SM).  When the grid would take a few waves at that size but
+// fits one wave with narrower CTAs, the narrower CTAs win (no wave tail).
+// V1 has only num_seqs * num_kv_heads CTAs, so it takes the widest CTA.
+void size_attn(AttnLaunch &L, int dev, int sms)
+{
+    const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
+    const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
     const size_t sb = stage_bytes(L.block_size);
+    int stages = tune_s > 0 ? tune_s : 2;
     while ((size_t)stages * sb < warp_scratch_bytes(L.p.group))
         ++stages;
-    while (1024 + (size_t)warps * stages * sb > kMaxSmem && stages > 1)
+    int warps;
+    if (tune_w > 0) {
+        warps = tune_w;
+    } else if (L.v1) {
+        warps = L.block_size == 16 ? 8 : 6;
+    } else {
+        const int w0 = L.block_size == 16 ? 4 : 2;
+        warps = w0;
+        const long long ctas = (long long)L.grid.x * L.grid.y * L.grid.z;
+        const long long occ0 = occupancy(dev, L, w0, stages);
+        if (occ0 > 0 && ctas > occ0 * sms && ctas <= 3 * occ0 * sms) {
+            for (int w1 = w0 / 2; w1 >= 1; w1 /= 2) {
+                if (ctas <= (long long)occupancy(dev, L, w1, stages) * sms) {
+                    warps = w1;
+                    break;
+                }
+            }
+        }
+    }
+    while (attn_smem(L.block_size, warps, stages) > kMaxSmem && stages > 1 &&
+           (size_t)(stages - 1) * sb >= warp_scratch_bytes(L.p.group))
         --stages;
-    while (1024 + (size_t)warps * stages * sb > kMaxSmem && warps > 1)
+    while (attn_smem(L.block_size, warps, stages) > kMaxSmem && warps > 1)
         --warps;
     L.warps = warps;
     L.p.stages = stages;
-    L.smem_bytes = 1024 + (size_t)warps * stages * sb;
+    L.smem_bytes = attn_smem(L.block_size, warps, stages);
 }
 
 int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
@@ -153,15 +254,12 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     int dev;
     if (current_device(&dev))
         return PA_ERR_CUDA;
-    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
-    if (g_smem_optin[dev][slot].load(std::memory_order_relaxed) < (int)L.smem_bytes) {
-        cudaError_t e = L.dtype == PA_BF16
-                            ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, L.smem_bytes)
-                            : attn_prepare_f16(L.block_size, L.p.group, L.v1, L.smem_bytes);
-        if (e != cudaSuccess)
-            return PA_ERR_CUDA;
-        g_smem_optin[dev][slot].store((int)L.smem_bytes, std::memory_order_relaxed);
-    }
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return PA_ERR_CUDA;
+    if (ensure_prepared(dev, L))
+        return PA_ERR_CUDA;
+    size_attn(L, dev, sms);
     cudaError_t e = L.dtype == PA_BF16 ? launch_attn_bf16(L, stream) : launch_attn_f16(L, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
@@ -203,7 +301,6 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     L.dtype = dtype;
     L.v1 = v1;
     L.grid = dim3(v1 ? 1 : num_partitions, num_kv_heads, num_seqs);
-    size_attn(L);
     return PA_OK;
 }
 
@@ -274,7 +371,13 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int hea
     p.max_logits = max_logits;
     p.out = out;
     p.status = status;
-    return launch_merge(dtype, p, num_seqs, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    int dev;
+    if (current_device(&dev))
+        return PA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return PA_ERR_CUDA;
+    return launch_merge(dtype, p, num_seqs, sms, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size, int sms)

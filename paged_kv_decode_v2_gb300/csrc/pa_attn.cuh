@@ -66,6 +66,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int kv = blockIdx.y;
     const int b = blockIdx.z;
 
+    // Let a merge grid launched after this one be scheduled early; it waits
+    // for this grid's completion before reading what it writes.
+    asm volatile("griddepcontrol.launch_dependents;");
+
     // ---- sequence range owned by this CTA
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {
@@ -436,6 +440,17 @@ static cudaError_t attn_prepare(int block_size, int group, bool v1, size_t smem_
 {
     return cudaFuncSetAttribute(attn_kernel_ptr<T>(block_size, group, v1),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+}
+
+// Resident CTAs per SM for a launch shape (0 on error).
+template <typename T>
+static int attn_occupancy_t(int block_size, int group, bool v1, int warps, size_t smem_bytes)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel_ptr<T>(block_size, group, v1),
+                                                      warps * 32, smem_bytes) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 template <typename T>

@@ -13,4 +13,9 @@ cudaError_t launch_attn_bf16(const AttnLaunch &L, cudaStream_t stream)
     return attn_launch<__nv_bfloat16>(L, stream);
 }
 
+int attn_occupancy_bf16(int block_size, int group, bool v1, int warps, size_t smem_bytes)
+{
+    return attn_occupancy_t<__nv_bfloat16>(block_size, group, v1, warps, smem_bytes);
+}
+
 } // namespace pa

@@ -12,7 +12,7 @@ constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 16;        // query heads per KV head
 constexpr int kMaxWarps = 8;         // warps per attention CTA
 constexpr int kMaxStages = 8;        // TMA ring stages per warp
-constexpr int kMergeThreads = 256;   // phase-2 CTA size
+constexpr int kMergeThreads = 128;   // phase-2 CTA size
 
 // Arguments of the attention kernel (phase 1 of V2, or V1).
 struct AttnParams {
@@ -75,7 +75,11 @@ cudaError_t launch_attn_f16(const AttnLaunch &L, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnLaunch &L, cudaStream_t stream);
 cudaError_t attn_prepare_f16(int block_size, int group, bool v1, size_t smem_bytes);
 cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, size_t smem_bytes);
-cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, cudaStream_t stream);
+cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
+                         cudaStream_t stream);
+int attn_occupancy(int dtype, int block_size, int group, bool v1, int warps, size_t smem_bytes);
+int attn_occupancy_f16(int block_size, int group, bool v1, int warps, size_t smem_bytes);
+int attn_occupancy_bf16(int block_size, int group, bool v1, int warps, size_t smem_bytes);
 cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns, cudaStream_t stream);
 
 } // namespace pa

@@ -6,98 +6,130 @@
 //     out        = sum_p (rescale_p / sum_q rescale_q) * tmp_output[p]
 // and the self-test kernel of the bounded wait.
 //
-// One CTA per (query head, sequence).  Warp w takes partitions w, w + 8, ...
-// and each lane 4 consecutive dims (one float4 per partition), so a warp
-// reads one 512-byte partition row per step; the eight warps' partial sums
-// meet in shared memory.
+// One CTA per (query head, sequence, slice of head_dim); the slice is the
+// whole head or a half or quarter of it when there are few (seq, head)
+// pairs.  A group of lanes owns one partition at a time and reads the
+// slice as float4s (contiguous bytes); the groups of a CTA take partitions
+// round robin and their running states meet in shared memory.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
-template <typename T>
+template <typename T, int DSPLIT>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p)
 {
     using E = Elem<T>;
-    constexpr int kWarps = kMergeThreads / 32;
-    __shared__ float4 s_acc[kWarps][32];
-    __shared__ float s_w[kWarps];
-    __shared__ float s_max[kWarps];
+    constexpr int kDims = kHeadDim / DSPLIT;       // dims of head_dim this CTA owns
+    constexpr int kGroup = kDims / 4;              // lanes per partition (one float4 each)
+    constexpr int kSlots = kMergeThreads / kGroup; // partitions in flight per CTA
+    __shared__ float s_m[kSlots];
+    __shared__ float s_l[kSlots];
+    __shared__ float4 s_acc[kSlots][kGroup];
 
     const int h = blockIdx.x;
     const int b = blockIdx.y;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
+    const int d0 = blockIdx.z * kDims;
+    const int slot = threadIdx.x / kGroup; // partitions slot, slot + kSlots, ...
+    const int c = threadIdx.x % kGroup;    // float4 column within the CTA's dims
 
+    // Inputs not written by phase 1 may be read before the dependency wait.
     int L = __ldg(&p.seq_lens[b]);
     L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
     const int np = (L + p.partition_size - 1) / p.partition_size;
     const size_t bh = (size_t)b * p.num_heads + h;
-    T *out = static_cast<T *>(p.out) + bh * kHeadDim;
+    T *out = static_cast<T *>(p.out) + bh * kHeadDim + d0;
     if (np == 0) {
-        if (threadIdx.x < kHeadDim)
+        if (threadIdx.x < kDims)
             out[threadIdx.x] = E::from_float(0.f);
         return;
     }
     const float *ml = p.max_logits + bh * p.max_num_partitions;
     const float *es = p.exp_sums + bh * p.max_num_partitions;
-    const float4 *tmp = reinterpret_cast<const float4 *>(p.tmp_output + bh * p.max_num_partitions * kHeadDim);
+    const float4 *tmp = reinterpret_cast<const float4 *>(p.tmp_output + bh * p.max_num_partitions * kHeadDim + d0);
 
-    // global_max
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < np; i += kMergeThreads)
-        mx = fmaxf(mx, __ldg(ml + i));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0)
-        s_max[warp] = mx;
-    __syncthreads();
-    float gmax = s_max[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w)
-        gmax = fmaxf(gmax, s_max[w]);
-    const float gmax2 = gmax * kLog2e;
+    // Phase 1's results are visible only after this point.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // sum_p rescale_p * o_p and sum_p rescale_p
+    // One pass over the partitions with a running maximum: the pages' rule
+    // rescale_p = exp(m_p - M) * l_p, with M raised as larger maxima appear
+    // and the partial sums multiplied by exp(M_old - M_new).
+    float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
 #pragma unroll 4
-    for (int i = warp; i < np; i += kWarps) {
-        const float w = fast_exp2(fmaf(__ldg(ml + i), kLog2e, -gmax2)) * __ldg(es + i);
-        const float4 v = __ldg(tmp + (size_t)i * (kHeadDim / 4) + lane);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
-        wsum += w;
+    for (int i = slot; i < np; i += kSlots) {
+        const float mp = __ldg(ml + i);
+        const float lp = __ldg(es + i);
+        const float4 v = __ldg(tmp + (size_t)i * (kHeadDim / 4) + c);
+        const float mn = fmaxf(m, mp);
+        const float a = fast_exp2((m - mn) * kLog2e); // 0 while m is -inf
+        const float w = fast_exp2((mp - mn) * kLog2e) * lp;
+        acc.x = fmaf(acc.x, a, w * v.x);
+        acc.y = fmaf(acc.y, a, w * v.y);
+        acc.z = fmaf(acc.z, a, w * v.z);
+        acc.w = fmaf(acc.w, a, w * v.w);
+        l = fmaf(l, a, w);
+        m = mn;
     }
-    s_acc[warp][lane] = acc;
-    if (lane == 0)
-        s_w[warp] = wsum;
+    s_acc[slot][c] = acc;
+    if (c == 0) {
+        s_m[slot] = m;
+        s_l[slot] = l;
+    }
     __syncthreads();
 
-    if (threadIdx.x < kHeadDim) {
+    if (threadIdx.x < kDims) {
         const int d = threadIdx.x;
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s)
+            M = fmaxf(M, s_m[s]);
         float total = 0.f, o = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            total += s_w[w];
-            const float *a = reinterpret_cast<const float *>(&s_acc[w][d >> 2]);
-            o += a[d & 3];
+        for (int s = 0; s < kSlots; ++s) {
+            const float f = s_m[s] == -INFINITY ? 0.f : fast_exp2((s_m[s] - M) * kLog2e);
+            total = fmaf(f, s_l[s], total);
+            const float *a = reinterpret_cast<const float *>(&s_acc[s][d >> 2]);
+            o = fmaf(f, a[d & 3], o);
         }
         out[d] = E::from_float(o / total);
     }
 }
 
-cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, cudaStream_t stream)
+template <typename T>
+static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dsplit, const MergeParams &p)
 {
-    dim3 grid(p.num_heads, num_seqs);
+    if (dsplit == 4)
+        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 4>, p);
+    if (dsplit == 2)
+        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 2>, p);
+    return cudaLaunchKernelEx(&cfg, merge_kernel<T, 1>, p);
+}
+
+cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
+                         cudaStream_t stream)
+{
+    // Split head_dim over 1, 2 or 4 CTAs so that the grid has at least about
+    // two CTAs per SM; a finer split only adds CTAs of very little work.
+    const long long pairs = (long long)p.num_heads * num_seqs;
+    int dsplit = 1;
+    while (dsplit < 4 && pairs * dsplit < 2LL * num_sms)
+        dsplit *= 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.num_heads, num_seqs, dsplit);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // attention grid before it drains; griddepcontrol.wait orders the reads.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (dtype == PA_BF16)
-        merge_kernel<__nv_bfloat16><<<grid, kMergeThreads, 0, stream>>>(p);
-    else
-        merge_kernel<__half><<<grid, kMergeThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+        return launch_merge_t<__nv_bfloat16>(cfg, dsplit, p);
+    return launch_merge_t<__half>(cfg, dsplit, p);
 }
 
 // One warp waits on a barrier that nothing completes; the bounded wait must

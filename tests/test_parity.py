@@ -60,7 +60,7 @@ def test_fuzz_grid(dtype, bs, G, P):
     full_check(wl.make_inputs(w, device="cuda"), P)
 
 
-@pytest.mark.parametrize("warps,stages", [(1, 1), (1, 2), (2, 4), (8, 2), (3, 3), (4, 8)])
+@pytest.mark.parametrize("warps,stages", [(1, 1), (1, 2), (2, 1), (2, 4), (8, 2), (3, 3), (4, 8)])
 def test_launch_shapes_do_not_change_results(cuda_lib, warps, stages):
     w = wl.Workload("shapes", 4, 16, 2, 128, 16, 256, wl.BF16, "list",
                     seq_lens=(1, 700, 2049, 4096), seed=55)
