@@ -16,7 +16,6 @@ using namespace pa;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kMaxSmem = 227 * 1024;
 
 std::atomic<int> g_tune_warps{0};
 std::atomic<int> g_tune_stages{0};
@@ -163,22 +162,30 @@ int kernel_slot(int dtype, int block_size, int group, bool v1)
     return (dtype == PA_BF16 ? 8 : 0) | (block_size == 32 ? 4 : 0) | (group > 8 ? 2 : 0) | (v1 ? 1 : 0);
 }
 
-// Per-device: kernel already opted in to the maximum dynamic shared memory.
-std::atomic<int> g_prepared[kMaxDevices][16];
-// Per-device resident CTAs per SM at two stages per warp, stored + 1 (0 = not queried).
-std::atomic<int> g_occ2[kMaxDevices][16][kMaxWarps + 1];
+// Per-device, per-kernel dynamic shared memory limit after the opt-in (0 = not yet).
+std::atomic<int> g_smem_limit[kMaxDevices][16];
+// Per-device resident CTAs per SM by [kernel][warps][stages], stored + 1 (0 = not queried).
+std::atomic<int> g_occ[kMaxDevices][16][kMaxWarps + 1][kMaxStages + 1];
 
-int ensure_prepared(int dev, const AttnLaunch &L)
+// Opts the kernel in to the device's largest dynamic shared memory (once per
+// device) and returns that limit, or 0 on error.
+size_t smem_limit(int dev, const AttnLaunch &L)
 {
     const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
-    if (g_prepared[dev][slot].load(std::memory_order_acquire))
-        return PA_OK;
-    cudaError_t e = L.dtype == PA_BF16 ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, kMaxSmem)
-                                       : attn_prepare_f16(L.block_size, L.p.group, L.v1, kMaxSmem);
+    const int have = g_smem_limit[dev][slot].load(std::memory_order_acquire);
+    if (have > 0)
+        return (size_t)have;
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    size_t limit = 0;
+    cudaError_t e = L.dtype == PA_BF16
+                        ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, optin, &limit)
+                        : attn_prepare_f16(L.block_size, L.p.group, L.v1, optin, &limit);
     if (e != cudaSuccess)
-        return PA_ERR_CUDA;
-    g_prepared[dev][slot].store(1, std::memory_order_release);
-    return PA_OK;
+        return 0;
+    g_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
+    return limit;
 }
 
 size_t attn_smem(int block_size, int warps, int stages)
@@ -186,38 +193,36 @@ size_t attn_smem(int block_size, int warps, int stages)
     return 1024 + (size_t)warps * stages * stage_bytes(block_size);
 }
 
-int occupancy(int dev, const AttnLaunch &L, int warps, int stages)
+int occupancy(int dev, const AttnLaunch &L, int warps, int stages, size_t limit)
 {
     const size_t smem = attn_smem(L.block_size, warps, stages);
-    if (smem > kMaxSmem)
+    if (smem > limit || warps < 1 || warps > kMaxWarps || stages < 1 || stages > kMaxStages)
         return 0;
     const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
-    if (stages == 2) {
-        const int c = g_occ2[dev][slot][warps].load(std::memory_order_relaxed);
-        if (c)
-            return c - 1;
-    }
+    const int c = g_occ[dev][slot][warps][stages].load(std::memory_order_relaxed);
+    if (c)
+        return c - 1;
     const int n = L.dtype == PA_BF16
                       ? attn_occupancy_bf16(L.block_size, L.p.group, L.v1, warps, smem)
                       : attn_occupancy_f16(L.block_size, L.p.group, L.v1, warps, smem);
-    if (stages == 2)
-        g_occ2[dev][slot][warps].store(n + 1, std::memory_order_relaxed);
+    g_occ[dev][slot][warps][stages].store(n + 1, std::memory_order_relaxed);
     return n;
 }
 
-// Launch shape of the attention kernel.  Each warp keeps two ring stages
-// (one block being computed, one landing): the sweep on GB300 showed that
-// more stages per warp only lose CTAs per SM.  Phase 1 uses 4 warps for
-// 16-token blocks and 2 for 32-token blocks (about 64 KB of shared memory,
-// three CTAs per SM).  When the grid would take a few waves at that size but
-// fits one wave with narrower CTAs, the narrower CTAs win (no wave tail).
-// V1 has only num_seqs * num_kv_heads CTAs, so it takes the widest CTA.
-void size_attn(AttnLaunch &L, int dev, int sms)
+// Launch shape of the attention kernel, from a warps x stages sweep on
+// GB300.  Phase 1 uses 4 warps per CTA and about 64 KB of shared memory, so
+// three CTAs share an SM: two ring stages per warp (one block computing, one
+// landing) for 16-token blocks, one stage for 32-token blocks (the twice
+// larger stage would otherwise halve the CTAs per SM).  When the grid would
+// take a few waves at that size but fits one wave with narrower CTAs, the
+// narrower CTAs win (no wave tail).  V1 has only num_seqs * num_kv_heads
+// CTAs, so it takes the widest CTA.
+void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
 {
     const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
     const size_t sb = stage_bytes(L.block_size);
-    int stages = tune_s > 0 ? tune_s : 2;
+    int stages = tune_s > 0 ? tune_s : (L.v1 || L.block_size == 16 ? 2 : 1);
     while ((size_t)stages * sb < warp_scratch_bytes(L.p.group))
         ++stages;
     int warps;
@@ -226,23 +231,23 @@ void size_attn(AttnLaunch &L, int dev, int sms)
     } else if (L.v1) {
         warps = L.block_size == 16 ? 8 : 6;
     } else {
-        const int w0 = L.block_size == 16 ? 4 : 2;
+        const int w0 = 4;
         warps = w0;
         const long long ctas = (long long)L.grid.x * L.grid.y * L.grid.z;
-        const long long occ0 = occupancy(dev, L, w0, stages);
+        const long long occ0 = occupancy(dev, L, w0, stages, limit);
         if (occ0 > 0 && ctas > occ0 * sms && ctas <= 3 * occ0 * sms) {
             for (int w1 = w0 / 2; w1 >= 1; w1 /= 2) {
-                if (ctas <= (long long)occupancy(dev, L, w1, stages) * sms) {
+                if (ctas <= (long long)occupancy(dev, L, w1, stages, limit) * sms) {
                     warps = w1;
                     break;
                 }
             }
         }
     }
-    while (attn_smem(L.block_size, warps, stages) > kMaxSmem && stages > 1 &&
+    while (attn_smem(L.block_size, warps, stages) > limit && stages > 1 &&
            (size_t)(stages - 1) * sb >= warp_scratch_bytes(L.p.group))
         --stages;
-    while (attn_smem(L.block_size, warps, stages) > kMaxSmem && warps > 1)
+    while (attn_smem(L.block_size, warps, stages) > limit && warps > 1)
         --warps;
     L.warps = warps;
     L.p.stages = stages;
@@ -257,9 +262,12 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     const int sms = sm_count(dev);
     if (sms <= 0)
         return PA_ERR_CUDA;
-    if (ensure_prepared(dev, L))
+    const size_t limit = smem_limit(dev, L);
+    if (limit == 0)
         return PA_ERR_CUDA;
-    size_attn(L, dev, sms);
+    size_attn(L, dev, sms, limit);
+    if (L.smem_bytes > limit)
+        return PA_ERR_UNSUPPORTED;
     cudaError_t e = L.dtype == PA_BF16 ? launch_attn_bf16(L, stream) : launch_attn_f16(L, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

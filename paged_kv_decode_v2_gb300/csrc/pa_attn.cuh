@@ -70,23 +70,50 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // for this grid's completion before reading what it writes.
     asm volatile("griddepcontrol.launch_dependents;");
 
+    // ---- loads that do not depend on the sequence length, issued together:
+    // the length, the first two chunks of block ids and the Q fragments.
+    const int head0 = kv * p.group;
+    const int blk0 = V1 ? 0 : part * p.part_blocks;
+    const int range_max = V1 ? p.max_blocks : min(p.part_blocks, p.max_blocks - blk0);
+    const int cnt_max = warp < range_max ? (range_max - warp + nwarps - 1) / nwarps : 0;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
+    const int Lraw = __ldg(&p.seq_lens[b]);
+    auto load_ids = [&](int chunk, int bound) -> int32_t {
+        const int i = chunk * 32 + lane;
+        return i < bound ? __ldg(bt_row + (size_t)nwarps * i) : 0;
+    };
+    int32_t ids_cur = load_ids(0, cnt_max);
+    int32_t ids_next = load_ids(1, cnt_max);
+
+    // Q^T fragments (B operand of S^T = K Q^T): head 8j + g4, dims 16ks + 2t4 (+1, +8, +9)
+    uint32_t qf[NT][8][2];
+    {
+        const uint32_t *q32 = static_cast<const uint32_t *>(p.query);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int g = j * 8 + g4;
+            const bool has = g < p.group;
+            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (kHeadDim / 2);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qf[j][ks][0] = has ? __ldg(q32 + rowbase + ks * 8 + t4) : 0u;
+                qf[j][ks][1] = has ? __ldg(q32 + rowbase + ks * 8 + 4 + t4) : 0u;
+            }
+        }
+    }
+
     // ---- sequence range owned by this CTA
-    int L = __ldg(&p.seq_lens[b]);
+    int L = Lraw;
     if (L < 0 || L > p.seq_len_cap) {
         if (threadIdx.x == 0 && part == 0 && kv == 0)
             set_status(p.status, PA_STATUS_BAD_SEQ_LEN);
         L = L < 0 ? 0 : p.seq_len_cap;
     }
-    int tok0 = 0, ntok = L;
-    if (!V1) {
-        tok0 = part * p.part_blocks * BS;
-        if (tok0 >= L)
-            return; // partition past the end of this sequence: nothing to write
-        ntok = min(p.part_blocks * BS, L - tok0);
-    }
+    const int tok0 = blk0 * BS;
+    if (!V1 && tok0 >= L)
+        return; // partition past the end of this sequence: nothing to write
+    const int ntok = V1 ? L : min(p.part_blocks * BS, L - tok0);
     const int nblk = (ntok + BS - 1) / BS;
-    const int blk0 = tok0 / BS;
-    const int head0 = kv * p.group;
 
     if (V1 && nblk == 0) { // empty sequence: zero output
         T *out = static_cast<T *>(p.out);
@@ -102,7 +129,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     // Blocks of this warp: j = warp + nwarps * i, i < cnt.
     const int cnt = warp < nblk ? (nblk - warp + nwarps - 1) / nwarps : 0;
-    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
 
     if (lane == 0) {
         for (int s = 0; s < stages; ++s)
@@ -117,14 +143,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     const uint64_t policy = l2_evict_first_policy();
     int32_t status_bits = 0;
-
-    // Block ids, a chunk of 32 per warp, with the next chunk in flight.
-    auto load_ids = [&](int chunk) -> int32_t {
-        const int i = chunk * 32 + lane;
-        return i < cnt ? __ldg(bt_row + (size_t)nwarps * i) : 0;
-    };
-    int32_t ids_cur = load_ids(0);
-    int32_t ids_next = load_ids(1);
     int chunk_cur = 0;
 
     // Issue the four TMA loads of the warp's i-th block into stage s (warp-uniform call).
@@ -132,7 +150,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const int c = i >> 5;
         if (c != chunk_cur) {
             ids_cur = ids_next;
-            ids_next = load_ids(c + 1);
+            ids_next = load_ids(c + 1, cnt);
             chunk_cur = c;
         }
         int32_t phys = __shfl_sync(0xffffffffu, ids_cur, i & 31);
@@ -155,23 +173,6 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     int issued = 0;
     for (; issued < cnt && issued < stages; ++issued)
         issue(issued, issued);
-
-    // ---- Q^T fragments (B operand of S^T = K Q^T): head 8j + g4, dims 16ks + 2t4 (+1, +8, +9)
-    uint32_t qf[NT][8][2];
-    {
-        const uint32_t *q32 = static_cast<const uint32_t *>(p.query);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int g = j * 8 + g4;
-            const bool has = g < p.group;
-            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (kHeadDim / 2);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                qf[j][ks][0] = has ? __ldg(q32 + rowbase + ks * 8 + t4) : 0u;
-                qf[j][ks][1] = has ? __ldg(q32 + rowbase + ks * 8 + 4 + t4) : 0u;
-            }
-        }
-    }
 
     // Running softmax state of this lane's heads 8j + 2t4 (+1): natural-log units.
     float m_run[NT][2], l_run[NT][2];
@@ -435,11 +436,20 @@ static const void *attn_kernel_ptr(int block_size, int group, bool v1)
 #undef PA_PICK
 }
 
+// Opts the kernel in to the largest dynamic shared memory the device allows
+// next to its static shared memory; returns that limit in *limit.
 template <typename T>
-static cudaError_t attn_prepare(int block_size, int group, bool v1, size_t smem_bytes)
+static cudaError_t attn_prepare(int block_size, int group, bool v1, int optin_bytes, size_t *limit)
 {
-    return cudaFuncSetAttribute(attn_kernel_ptr<T>(block_size, group, v1),
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+    const void *fn = attn_kernel_ptr<T>(block_size, group, v1);
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess)
+        return e;
+    if ((size_t)optin_bytes <= fa.sharedSizeBytes)
+        return cudaErrorInvalidValue;
+    *limit = (size_t)optin_bytes - fa.sharedSizeBytes;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*limit);
 }
 
 // Resident CTAs per SM for a launch shape (0 on error).

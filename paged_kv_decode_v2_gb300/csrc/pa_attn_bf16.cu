@@ -3,9 +3,9 @@
 
 namespace pa {
 
-cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, size_t smem_bytes)
+cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, int optin_bytes, size_t *limit)
 {
-    return attn_prepare<__nv_bfloat16>(block_size, group, v1, smem_bytes);
+    return attn_prepare<__nv_bfloat16>(block_size, group, v1, optin_bytes, limit);
 }
 
 cudaError_t launch_attn_bf16(const AttnLaunch &L, cudaStream_t stream)

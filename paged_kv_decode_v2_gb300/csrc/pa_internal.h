@@ -73,8 +73,8 @@ inline size_t warp_scratch_bytes(int group)
 
 cudaError_t launch_attn_f16(const AttnLaunch &L, cudaStream_t stream);
 cudaError_t launch_attn_bf16(const AttnLaunch &L, cudaStream_t stream);
-cudaError_t attn_prepare_f16(int block_size, int group, bool v1, size_t smem_bytes);
-cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, size_t smem_bytes);
+cudaError_t attn_prepare_f16(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
+cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
                          cudaStream_t stream);
 int attn_occupancy(int dtype, int block_size, int group, bool v1, int warps, size_t smem_bytes);
