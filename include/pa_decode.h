@@ -205,6 +205,44 @@ PA_API int pa_decode(const void *query, const void *key_cache, const void *value
  */
 PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
 
+/*
+ * Size of the intermediates array that pa_decode_v2_static keeps inside the
+ * library: 16 MiB of device memory on every GPU that loads the library,
+ * held until the process exits.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * pa_decode_v2 for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for callers that must
+ * not or cannot call cudaMalloc -- code inside a host framework that owns
+ * every device allocation, runtimes handed a fixed memory budget up front,
+ * or hot paths where an allocation (and the implicit device synchronisation
+ * it brings) is not allowed.  The caller passes only inputs and outputs,
+ * with the same meaning as in pa_decode_v2; tmp_output, exp_sums and
+ * max_logits live in a PA_STATIC_SCRATCH_BYTES array owned by the library.
+ * Nothing is allocated or freed by this call.
+ *   - Limit: num_seqs * num_heads * ceil(L / partition_size) *
+ *     (head_dim + 2) * 4 bytes must fit in PA_STATIC_SCRATCH_BYTES, where L
+ *     is max_seq_len_hint if > 0, else max_blocks_per_seq * block_size.
+ *     Larger calls return PA_ERR_WORKSPACE and launch nothing.
+ *   - Set-up: the first call on a device looks up the array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's contents.  No slot needs clearing (each slot the merge
+ *     reads is written earlier in the same call), but two calls that
+ *     overlap on the GPU (different streams, or different host threads)
+ *     race on the array and corrupt each other's results: keep such calls
+ *     ordered on one stream.
+ */
+PA_API int pa_decode_v2_static(const void *query, const void *key_cache, const void *value_cache,
+                               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                               int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                               int block_size, int max_blocks_per_seq, int max_seq_len_hint,
+                               float scale, int partition_size, int dtype, void *out,
+                               int32_t *status, pa_stream_t stream);
+
 /* Human-readable name of a PA_* return code (static string). */
 PA_API const char *pa_status_string(int code);
 

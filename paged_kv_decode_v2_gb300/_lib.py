@@ -198,3 +198,23 @@ def pa_set_launch_config(warps_per_cta: int = 0, stages_per_warp: int = 0) -> No
 def pa_selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:
     _check("pa_selftest_wait_timeout",
            load().pa_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)))
+
+
+def pa_decode_v2_static(query, key_cache, value_cache, block_tables, seq_lens, scale,
+                        partition_size, out, max_seq_len_hint=0, status=None, stream=None):
+    """pa_decode_v2 with the intermediates kept in the library's own device array.
+
+    For callers that cannot allocate device memory themselves; see
+    pa_decode_v2_static in include/pa_decode.h for the size limit and for why
+    concurrent calls must not overlap on the GPU.
+    """
+    lib = load()
+    fn = lib.pa_decode_v2_static
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P, P]
+    fn.restype = I
+    args = _shape_args(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint, scale)
+    rc = fn(*args, int(partition_size), _DTYPE[query.dtype], _ptr(out), _ptr(status),
+            _stream(stream))
+    _check("pa_decode_v2_static", rc)
+    return out
