@@ -66,8 +66,15 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int kv = blockIdx.y;
     const int b = blockIdx.z;
 
-    // Let a merge grid launched after this one be scheduled early; it waits
-    // for this grid's completion before reading what it writes.
+    // This grid is launched with programmatic stream serialisation, so its
+    // CTAs may become resident while the kernel before it in the stream is
+    // still running.  Nothing global is read or written before this wait,
+    // which returns once that kernel has completed and its writes are
+    // visible.  Then the grid after this one (the merge) may be scheduled
+    // early; it waits the same way before reading what this grid writes.
+    if (threadIdx.x == 0)
+        prefetch_tensormap(&tmap_k);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
 
     // ---- loads that do not depend on the sequence length, issued together:
@@ -469,7 +476,17 @@ static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
     const void *fn = attn_kernel_ptr<T>(L.block_size, L.p.group, L.v1);
     void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
                     const_cast<AttnParams *>(&L.p)};
-    return cudaLaunchKernel(fn, L.grid, dim3(L.warps * 32), args, L.smem_bytes, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = dim3(L.warps * 32);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 } // namespace pa

@@ -7,7 +7,7 @@
 // and the self-test kernel of the bounded wait.
 //
 // One CTA per (query head, sequence, slice of head_dim); the slice is the
-// whole head or a half or quarter of it when there are few (seq, head)
+// whole head or a half, quarter or eighth of it when there are few (seq, head)
 // pairs.  A group of lanes owns one partition at a time and reads the
 // slice as float4s (contiguous bytes); the groups of a CTA take partitions
 // round robin and their running states meet in shared memory.
@@ -33,6 +33,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int slot = threadIdx.x / kGroup; // partitions slot, slot + kSlots, ...
     const int c = threadIdx.x % kGroup;    // float4 column within the CTA's dims
 
+    // The next call's attention grid may be scheduled while this one runs; it
+    // waits for this grid's completion before it touches global memory.
+    asm volatile("griddepcontrol.launch_dependents;");
     // Inputs not written by phase 1 may be read before the dependency wait.
     int L = __ldg(&p.seq_lens[b]);
     L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
@@ -99,6 +102,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 template <typename T>
 static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dsplit, const MergeParams &p)
 {
+    if (dsplit == 8)
+        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 8>, p);
     if (dsplit == 4)
         return cudaLaunchKernelEx(&cfg, merge_kernel<T, 4>, p);
     if (dsplit == 2)
@@ -109,11 +114,11 @@ static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dsplit, const Mer
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
                          cudaStream_t stream)
 {
-    // Split head_dim over 1, 2 or 4 CTAs so that the grid has at least about
-    // two CTAs per SM; a finer split only adds CTAs of very little work.
+    // Split head_dim over 1, 2, 4 or 8 CTAs so that the grid has at least
+    // about two CTAs per SM; a finer split only adds CTAs of very little work.
     const long long pairs = (long long)p.num_heads * num_seqs;
     int dsplit = 1;
-    while (dsplit < 4 && pairs * dsplit < 2LL * num_sms)
+    while (dsplit < 8 && pairs * dsplit < 2LL * num_sms)
         dsplit *= 2;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_heads, num_seqs, dsplit);
