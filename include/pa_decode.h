@@ -47,7 +47,7 @@
  *   Partition slots p >= ceil(seq_lens[b]/partition_size) are left untouched.
  *   A sequence with seq_len 0 gets a zero output row.
  *
- * Supported shapes: head_dim == 128; block_size 16 or 32;
+ * Supported shapes: head_dim 64, 128 or 256; block_size 16, 32 or 64;
  * partition_size a positive multiple of block_size; G = num_heads /
  * num_kv_heads an integer in [1, 16].  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned

@@ -75,9 +75,9 @@ int check_shape(const void *query, const void *key_cache, const void *value_cach
         return PA_ERR_INVALID_ARG;
     if (!std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
-    if (head_dim != kHeadDim)
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return PA_ERR_UNSUPPORTED;
-    if (block_size != 16 && block_size != 32)
+    if (block_size != 16 && block_size != 32 && block_size != 64)
         return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > kMaxGroup)
         return PA_ERR_UNSUPPORTED;
@@ -98,17 +98,18 @@ int seq_cap(int max_blocks_per_seq, int block_size, int hint)
     return (hint > 0 && hint < full) ? hint : full;
 }
 
-// 3-D view of a cache for the TMA: dims {64 (inner half of head_dim), 2 (halves),
-// rows = num_blocks * KV * block_size}, 128-byte swizzle, box {64, 1, block_size}.
+// 3-D view of a cache for the TMA: dims {64 (a slice of head_dim), head_dim / 64
+// (slices), rows = num_blocks * KV * block_size}, 128-byte swizzle, box
+// {64, 1, block_size}: one load brings one 64-dim slice of a block's tile.
 int encode_cache_map_uncached(CUtensorMap *map, const void *base, int dtype, int num_blocks,
-                              int num_kv_heads, int block_size)
+                              int num_kv_heads, int block_size, int head_dim)
 {
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
     if (!fn)
         return PA_ERR_CUDA;
     const cuuint64_t rows = (cuuint64_t)num_blocks * num_kv_heads * block_size;
-    const cuuint64_t dims[3] = {64, 2, rows};
-    const cuuint64_t strides[2] = {128, 256}; // bytes of dim 1 and dim 2
+    const cuuint64_t dims[3] = {64, (cuuint64_t)head_dim / 64, rows};
+    const cuuint64_t strides[2] = {128, (cuuint64_t)head_dim * 2}; // bytes of dim 1 and dim 2
     const cuuint32_t box[3] = {64, 1, (cuuint32_t)block_size};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType dt =
@@ -124,7 +125,7 @@ int encode_cache_map_uncached(CUtensorMap *map, const void *base, int dtype, int
 struct MapCacheEntry {
     CUtensorMap map;
     const void *base;
-    int dtype, num_blocks, num_kv_heads, block_size;
+    int dtype, num_blocks, num_kv_heads, block_size, head_dim;
     bool valid;
 };
 constexpr int kMapCacheSize = 8;
@@ -132,17 +133,19 @@ thread_local MapCacheEntry t_map_cache[kMapCacheSize];
 thread_local int t_map_next = 0;
 
 int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
-                     int num_kv_heads, int block_size)
+                     int num_kv_heads, int block_size, int head_dim)
 {
     for (int i = 0; i < kMapCacheSize; ++i) {
         const MapCacheEntry &e = t_map_cache[i];
         if (e.valid && e.base == base && e.dtype == dtype && e.num_blocks == num_blocks &&
-            e.num_kv_heads == num_kv_heads && e.block_size == block_size) {
+            e.num_kv_heads == num_kv_heads && e.block_size == block_size &&
+            e.head_dim == head_dim) {
             *map = e.map;
             return PA_OK;
         }
     }
-    int rc = encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size);
+    int rc = encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size,
+                                       head_dim);
     if (rc)
         return rc;
     MapCacheEntry &e = t_map_cache[t_map_next];
@@ -153,25 +156,32 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_bloc
     e.num_blocks = num_blocks;
     e.num_kv_heads = num_kv_heads;
     e.block_size = block_size;
+    e.head_dim = head_dim;
     e.valid = true;
     return PA_OK;
 }
 
-int kernel_slot(int dtype, int block_size, int group, bool v1)
+// Index of a kernel instantiation: storage type x head_dim x block size x n-tiles x V1/V2.
+constexpr int kKernelSlots = 2 * 3 * 3 * 2 * 2;
+
+int kernel_slot(int dtype, int head_dim, int block_size, int group, bool v1)
 {
-    return (dtype == PA_BF16 ? 8 : 0) | (block_size == 32 ? 4 : 0) | (group > 8 ? 2 : 0) | (v1 ? 1 : 0);
+    const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+    const int bi = block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
+    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (group > 8 ? 1 : 0)) * 2 +
+           (v1 ? 1 : 0);
 }
 
 // Per-device, per-kernel dynamic shared memory limit after the opt-in (0 = not yet).
-std::atomic<int> g_smem_limit[kMaxDevices][16];
+std::atomic<int> g_smem_limit[kMaxDevices][kKernelSlots];
 // Per-device resident CTAs per SM by [kernel][warps][stages], stored + 1 (0 = not queried).
-std::atomic<int> g_occ[kMaxDevices][16][kMaxWarps + 1][kMaxStages + 1];
+std::atomic<int> g_occ[kMaxDevices][kKernelSlots][kMaxWarps + 1][kMaxStages + 1];
 
 // Opts the kernel in to the device's largest dynamic shared memory (once per
 // device) and returns that limit, or 0 on error.
 size_t smem_limit(int dev, const AttnLaunch &L)
 {
-    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
+    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.p.group, L.v1);
     const int have = g_smem_limit[dev][slot].load(std::memory_order_acquire);
     if (have > 0)
         return (size_t)have;
@@ -179,59 +189,60 @@ size_t smem_limit(int dev, const AttnLaunch &L)
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 0;
     size_t limit = 0;
-    cudaError_t e = L.dtype == PA_BF16
-                        ? attn_prepare_bf16(L.block_size, L.p.group, L.v1, optin, &limit)
-                        : attn_prepare_f16(L.block_size, L.p.group, L.v1, optin, &limit);
+    cudaError_t e = attn_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.p.group, L.v1, optin,
+                                                           &limit);
     if (e != cudaSuccess)
         return 0;
     g_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
     return limit;
 }
 
-size_t attn_smem(int block_size, int warps, int stages)
+size_t attn_smem(const AttnLaunch &L, int warps, int stages)
 {
-    return 1024 + (size_t)warps * stages * stage_bytes(block_size);
+    return 1024 + (size_t)warps * stages * stage_bytes(L.block_size, L.head_dim);
 }
 
 int occupancy(int dev, const AttnLaunch &L, int warps, int stages, size_t limit)
 {
-    const size_t smem = attn_smem(L.block_size, warps, stages);
+    const size_t smem = attn_smem(L, warps, stages);
     if (smem > limit || warps < 1 || warps > kMaxWarps || stages < 1 || stages > kMaxStages)
         return 0;
-    const int slot = kernel_slot(L.dtype, L.block_size, L.p.group, L.v1);
+    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.p.group, L.v1);
     const int c = g_occ[dev][slot][warps][stages].load(std::memory_order_relaxed);
     if (c)
         return c - 1;
-    const int n = L.dtype == PA_BF16
-                      ? attn_occupancy_bf16(L.block_size, L.p.group, L.v1, warps, smem)
-                      : attn_occupancy_f16(L.block_size, L.p.group, L.v1, warps, smem);
+    const int n = attn_ops(L.dtype, L.head_dim)->occupancy(L.block_size, L.p.group, L.v1, warps, smem);
     g_occ[dev][slot][warps][stages].store(n + 1, std::memory_order_relaxed);
     return n;
 }
 
 // Launch shape of the attention kernel, from a warps x stages sweep on
-// GB300.  Phase 1 uses 4 warps per CTA and about 64 KB of shared memory, so
-// three CTAs share an SM: two ring stages per warp (one block computing, one
-// landing) for 16-token blocks, one stage for 32-token blocks (the twice
-// larger stage would otherwise halve the CTAs per SM).  When the grid would
-// take a few waves at that size but fits one wave with narrower CTAs, the
+// GB300.  Phase 1 aims at about 64 KB of ring per CTA (three CTAs per SM)
+// with 4 warps when a stage is small enough: two stages per warp (one block
+// computing, one landing) for stages up to 8 KB (16-token blocks of 128
+// dims), one stage beyond (a larger stage would otherwise cut the CTAs per
+// SM), and fewer warps for 32 KB and 64 KB stages.  When the grid would take
+// a few waves at that size but fits one wave with narrower CTAs, the
 // narrower CTAs win (no wave tail).  V1 has only num_seqs * num_kv_heads
-// CTAs, so it takes the widest CTA.
+// CTAs, so it takes the widest CTA that fits about 200 KB with two stages.
 void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
 {
     const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
-    const size_t sb = stage_bytes(L.block_size);
-    int stages = tune_s > 0 ? tune_s : (L.v1 || L.block_size == 16 ? 2 : 1);
-    while ((size_t)stages * sb < warp_scratch_bytes(L.p.group))
+    const size_t sb = stage_bytes(L.block_size, L.head_dim);
+    const size_t scratch = warp_scratch_bytes(L.p.group, L.head_dim);
+    auto clampi = [](long long v, int lo, int hi) { return (int)(v < lo ? lo : v > hi ? hi : v); };
+    const int w_fit = clampi((long long)(65536 / sb), 1, 4);
+    int stages = tune_s > 0 ? tune_s : (L.v1 ? 2 : clampi((long long)(65536 / (w_fit * sb)), 1, 2));
+    while ((size_t)stages * sb < scratch)
         ++stages;
     int warps;
     if (tune_w > 0) {
         warps = tune_w;
     } else if (L.v1) {
-        warps = L.block_size == 16 ? 8 : 6;
+        warps = clampi((long long)(200 * 1024 / (2 * sb)), 1, kMaxWarps);
     } else {
-        const int w0 = 4;
+        const int w0 = w_fit;
         warps = w0;
         const long long ctas = (long long)L.grid.x * L.grid.y * L.grid.z;
         const long long occ0 = occupancy(dev, L, w0, stages, limit);
@@ -244,14 +255,13 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
             }
         }
     }
-    while (attn_smem(L.block_size, warps, stages) > limit && stages > 1 &&
-           (size_t)(stages - 1) * sb >= warp_scratch_bytes(L.p.group))
+    while (attn_smem(L, warps, stages) > limit && stages > 1 && (size_t)(stages - 1) * sb >= scratch)
         --stages;
-    while (attn_smem(L.block_size, warps, stages) > limit && warps > 1)
+    while (attn_smem(L, warps, stages) > limit && warps > 1)
         --warps;
     L.warps = warps;
     L.p.stages = stages;
-    L.smem_bytes = attn_smem(L.block_size, warps, stages);
+    L.smem_bytes = attn_smem(L, warps, stages);
 }
 
 int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
@@ -268,23 +278,26 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     size_attn(L, dev, sms, limit);
     if (L.smem_bytes > limit)
         return PA_ERR_UNSUPPORTED;
-    cudaError_t e = L.dtype == PA_BF16 ? launch_attn_bf16(L, stream) : launch_attn_f16(L, stream);
+    cudaError_t e = attn_ops(L.dtype, L.head_dim)->launch(L, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 // Builds the attention launch (V2 phase 1 or V1) after validation.
 int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const void *value_cache,
                const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
-               int num_kv_heads, int num_blocks, int block_size, int max_blocks_per_seq, int cap,
-               float scale, int dtype, bool v1, int num_partitions, int partition_size,
+               int num_kv_heads, int head_dim, int num_blocks, int block_size,
+               int max_blocks_per_seq, int cap, float scale, int dtype, bool v1,
+               int num_partitions, int partition_size,
                float *tmp_output, float *exp_sums, float *max_logits, int max_num_partitions,
                void *out, int32_t *status)
 {
     std::memset(&L, 0, sizeof(L));
-    int rc = encode_cache_map(&L.tmap_k, key_cache, dtype, num_blocks, num_kv_heads, block_size);
+    int rc = encode_cache_map(&L.tmap_k, key_cache, dtype, num_blocks, num_kv_heads, block_size,
+                              head_dim);
     if (rc)
         return rc;
-    rc = encode_cache_map(&L.tmap_v, value_cache, dtype, num_blocks, num_kv_heads, block_size);
+    rc = encode_cache_map(&L.tmap_v, value_cache, dtype, num_blocks, num_kv_heads, block_size,
+                          head_dim);
     if (rc)
         return rc;
     AttnParams &p = L.p;
@@ -305,6 +318,7 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.max_logits = max_logits;
     p.out = out;
     p.status = status;
+    L.head_dim = head_dim;
     L.block_size = block_size;
     L.dtype = dtype;
     L.v1 = v1;
@@ -340,7 +354,8 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
         return PA_OK;
     AttnLaunch L;
     rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                    num_kv_heads, num_blocks, block_size, max_blocks_per_seq, cap, scale, dtype,
+                    num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, cap, scale,
+                    dtype,
                     false, np, partition_size, tmp_output, exp_sums, max_logits,
                     max_num_partitions, nullptr, status);
     if (rc)
@@ -360,7 +375,7 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int hea
         return PA_ERR_INVALID_ARG;
     if (dtype != PA_F16 && dtype != PA_BF16)
         return PA_ERR_INVALID_ARG;
-    if (head_dim != kHeadDim)
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_heads > INT32_MAX / 2)
         return PA_ERR_UNSUPPORTED;
@@ -371,6 +386,7 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int hea
     MergeParams p;
     p.seq_lens = seq_lens;
     p.num_heads = num_heads;
+    p.head_dim = head_dim;
     p.seq_len_cap = max_seq_len;
     p.partition_size = partition_size;
     p.max_num_partitions = max_num_partitions;
@@ -486,7 +502,8 @@ PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *va
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     AttnLaunch L;
     rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                    num_kv_heads, num_blocks, block_size, max_blocks_per_seq, cap, scale, dtype,
+                    num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, cap, scale,
+                    dtype,
                     true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
     if (rc)
         return rc;

@@ -10,8 +10,8 @@
 // Data movement.  Each warp of the CTA owns a private ring of `stages`
 // shared-memory stages and walks the blocks j = warp, warp + W, ... of the
 // CTA's range.  A stage holds one paged block's K tile and V tile
-// (block_size rows x 128 dims each), brought in by four TMA tensor loads
-// (K and V, two 64-dim halves) that complete on the stage's mbarrier.  The
+// (block_size rows x head_dim each), brought in by TMA tensor loads (one per
+// 64-dim slice of K and of V) that complete on the stage's mbarrier.  The
 // block id is read from the block table a full chunk of 32 blocks ahead of
 // use.  Loads use 128-byte swizzling, so the ldmatrix reads below touch 32
 // distinct banks.
@@ -19,8 +19,8 @@
 // Math (fp32 accumulation on the tensor cores, mma.sync m16n8k16).  Tokens
 // are the M dimension and query heads the N dimension (8 per n-tile), so a
 // GQA group of 8 fills an n-tile exactly:
-//     S^T[16 tokens x 8 heads]  = K_tile[16 x 128] . Q^T[128 x 8]   (8 MMAs)
-//     O^T[128 x 8 heads]       += V_tile^T[128 x 16] . P^T[16 x 8]  (8 MMAs)
+//     S^T[16 tokens x 8 heads]  = K_tile[16 x D] . Q^T[D x 8]   (D/16 MMAs)
+//     O^T[D x 8 heads]         += V_tile^T[D x 16] . P^T[16 x 8] (D/16 MMAs)
 // Q^T lives in registers for the whole CTA.  The S^T accumulator fragment is
 // turned into the P^T operand fragment with two movmatrix transposes.  The
 // softmax is the streaming {m, l, o} accumulator with the merge factor
@@ -40,16 +40,19 @@
 
 namespace pa {
 
-template <typename T, int BS, int NT, bool V1>
+template <typename T, int D, int BS, int NT, bool V1>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
 {
     using E = Elem<T>;
-    constexpr uint32_t kHalfBytes = BS * 128;      // one 64-dim half of a tile
-    constexpr uint32_t kStageBytes = 4 * kHalfBytes; // K0 K1 V0 V1
-    constexpr int kTiles = BS / 16;                  // 16-row MMA tiles per block
+    constexpr int kKS = D / 16;                       // 16-dim steps of Q.K, 16-dim tiles of O
+    constexpr int kSlices = D / 64;                   // 64-dim slices: one TMA load each
+    constexpr uint32_t kHalfBytes = BS * 128;         // one 64-dim slice of a K or V tile
+    constexpr uint32_t kStageBytes = 2 * kSlices * kHalfBytes; // K slices, then V slices
+    constexpr int kTiles = BS / 16;                   // 16-row MMA tiles per block
     constexpr int kHeads = NT * 8;
+    constexpr int kScr = D + 4;                       // scratch row stride (floats)
 
     __shared__ uint64_t bars[kMaxWarps * kMaxStages];
     __shared__ float s_factor[kMaxWarps][kMaxGroup];
@@ -93,16 +96,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     int32_t ids_next = load_ids(1, cnt_max);
 
     // Q^T fragments (B operand of S^T = K Q^T): head 8j + g4, dims 16ks + 2t4 (+1, +8, +9)
-    uint32_t qf[NT][8][2];
+    uint32_t qf[NT][kKS][2];
     {
         const uint32_t *q32 = static_cast<const uint32_t *>(p.query);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int g = j * 8 + g4;
             const bool has = g < p.group;
-            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (kHeadDim / 2);
+            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (D / 2);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
+            for (int ks = 0; ks < kKS; ++ks) {
                 qf[j][ks][0] = has ? __ldg(q32 + rowbase + ks * 8 + t4) : 0u;
                 qf[j][ks][1] = has ? __ldg(q32 + rowbase + ks * 8 + 4 + t4) : 0u;
             }
@@ -124,8 +127,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     if (V1 && nblk == 0) { // empty sequence: zero output
         T *out = static_cast<T *>(p.out);
-        for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += blockDim.x)
-            out[((size_t)b * p.num_heads + head0) * kHeadDim + idx] = E::from_float(0.f);
+        for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x)
+            out[((size_t)b * p.num_heads + head0) * D + idx] = E::from_float(0.f);
         return;
     }
 
@@ -170,10 +173,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             const uint32_t dst = ring + (uint32_t)s * kStageBytes;
             const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
             mbar_arrive_expect_tx(bar, kStageBytes);
-            tma_load_3d(dst, &tmap_k, 0, 0, row, bar, policy);
-            tma_load_3d(dst + kHalfBytes, &tmap_k, 0, 1, row, bar, policy);
-            tma_load_3d(dst + 2 * kHalfBytes, &tmap_v, 0, 0, row, bar, policy);
-            tma_load_3d(dst + 3 * kHalfBytes, &tmap_v, 0, 1, row, bar, policy);
+#pragma unroll
+            for (int sl = 0; sl < kSlices; ++sl)
+                tma_load_3d(dst + sl * kHalfBytes, &tmap_k, 0, sl, row, bar, policy);
+#pragma unroll
+            for (int sl = 0; sl < kSlices; ++sl)
+                tma_load_3d(dst + (kSlices + sl) * kHalfBytes, &tmap_v, 0, sl, row, bar, policy);
         }
     };
 
@@ -183,13 +188,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     // Running softmax state of this lane's heads 8j + 2t4 (+1): natural-log units.
     float m_run[NT][2], l_run[NT][2];
-    float o[NT][8][4];
+    float o[NT][kKS][4];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         m_run[j][0] = m_run[j][1] = -INFINITY;
         l_run[j][0] = l_run[j][1] = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
+        for (int mt = 0; mt < kKS; ++mt)
             o[j][mt][0] = o[j][mt][1] = o[j][mt][2] = o[j][mt][3] = 0.f;
     }
 
@@ -215,15 +220,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const int jblk = warp + nwarps * i;
         const int valid = min(BS, ntok - jblk * BS);
         const uint32_t kbase = ring + (uint32_t)s * kStageBytes;
-        const uint32_t vbase = kbase + 2 * kHalfBytes;
+        const uint32_t vbase = kbase + kSlices * kHalfBytes;
 
         if (valid < BS) {
             // Rows past the end of the sequence: zero V so no stale value reaches P.V.
-            const int nchunks = (BS - valid) * 16;
+            // A row is kSlices lines of eight 16-byte chunks.
+            const int nchunks = (BS - valid) * kSlices * 8;
             for (int c = lane; c < nchunks; c += 32) {
-                const int r = valid + (c >> 4);
-                const int h = (c >> 3) & 1;
-                st_shared_zero16(vbase + h * kHalfBytes + r * 128 + (c & 7) * 16);
+                const int r = valid + c / (kSlices * 8);
+                const int sl = (c >> 3) % kSlices;
+                st_shared_zero16(vbase + sl * kHalfBytes + r * 128 + (c & 7) * 16);
             }
             __syncwarp();
         }
@@ -233,12 +239,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             if (tile * 16 >= valid)
                 break;
             // ---- S^T = K_tile Q^T
-            uint32_t ka[8][4];
+            uint32_t ka[kKS][4];
             {
                 const int r = tile * 16 + k_row;
                 const uint32_t rbase = kbase + r * 128;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
+                for (int ks = 0; ks < kKS; ++ks) {
                     const int chunk = ((ks & 3) << 1) | k_chunk_hi;
                     ldsm_x4(rbase + (ks >> 2) * kHalfBytes + ((chunk ^ mrow) << 4), ka[ks]);
                 }
@@ -249,7 +255,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 float e[4] = {0.f, 0.f, 0.f, 0.f};
                 float f[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int ks = 0; ks < 8; ks += 2) {
+                for (int ks = 0; ks < kKS; ks += 2) {
                     E::mma(e, ka[ks], qf[j][ks][0], qf[j][ks][1]);
                     E::mma(f, ka[ks + 1], qf[j][ks + 1][0], qf[j][ks + 1][1]);
                 }
@@ -292,7 +298,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 l_run[j][0] = fmaf(l_run[j][0], a0, pv[0] + pv[2]);
                 l_run[j][1] = fmaf(l_run[j][1], a1, pv[1] + pv[3]);
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
+                for (int mt = 0; mt < kKS; ++mt) {
                     o[j][mt][0] *= a0;
                     o[j][mt][1] *= a1;
                     o[j][mt][2] *= a0;
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 const int r = tile * 16 + v_row;
                 const uint32_t rbase = vbase + r * 128;
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
+                for (int mt = 0; mt < kKS; ++mt) {
                     uint32_t va[4];
                     const int chunk = ((mt & 3) << 1) | v_chunk_lo;
                     ldsm_x4_trans(rbase + (mt >> 2) * kHalfBytes + ((chunk ^ mrow) << 4), va);
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     float *scr = reinterpret_cast<float *>(dyn_smem + (ring - smem_addr(dyn_smem)));
     float *scr_m = scr;
     float *scr_l = scr + kHeads;
-    float *scr_o = scr + 2 * kHeads; // [kHeads][132]
+    float *scr_o = scr + 2 * kHeads; // [kHeads][kScr]
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         const int hA = j * 8 + 2 * t4;
@@ -370,12 +376,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             scr_l[hA + 1] = l_run[j][1];
         }
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
+        for (int mt = 0; mt < kKS; ++mt) {
             const int d = mt * 16 + g4;
-            scr_o[hA * 132 + d] = o[j][mt][0];
-            scr_o[(hA + 1) * 132 + d] = o[j][mt][1];
-            scr_o[hA * 132 + d + 8] = o[j][mt][2];
-            scr_o[(hA + 1) * 132 + d + 8] = o[j][mt][3];
+            scr_o[hA * kScr + d] = o[j][mt][0];
+            scr_o[(hA + 1) * kScr + d] = o[j][mt][1];
+            scr_o[hA * kScr + d + 8] = o[j][mt][2];
+            scr_o[(hA + 1) * kScr + d + 8] = o[j][mt][3];
         }
     }
     __syncthreads();
@@ -400,20 +406,20 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < p.group * kHeadDim; idx += blockDim.x) {
-        const int h = idx >> 7;
-        const int d = idx & 127;
+    for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
+        const int h = idx / D;
+        const int d = idx % D;
         float acc = 0.f;
         for (int w = 0; w < nwarps; ++w)
-            acc = fmaf(s_factor[w][h], scr0[w * warp_stride + 2 * kHeads + h * 132 + d], acc);
+            acc = fmaf(s_factor[w][h], scr0[w * warp_stride + 2 * kHeads + h * kScr + d], acc);
         const float lsum = s_stat[1][h];
         const float val = acc / lsum;
         const size_t bh = (size_t)b * p.num_heads + head0 + h;
         if (V1) {
-            static_cast<T *>(p.out)[bh * kHeadDim + d] = E::from_float(val);
+            static_cast<T *>(p.out)[bh * D + d] = E::from_float(val);
         } else {
             const size_t slot = bh * p.max_num_partitions + part;
-            p.tmp_output[slot * kHeadDim + d] = val;
+            p.tmp_output[slot * D + d] = val;
             if (d == 0) {
                 p.exp_sums[slot] = lsum;
                 p.max_logits[slot] = s_stat[0][h];
@@ -422,33 +428,34 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
 }
 
-// Kernel dispatch on block size, n-tiles (G <= 8 or <= 16) and V1/V2.
-template <typename T>
+// Kernel dispatch on block size, n-tiles (G <= 8 or <= 16) and V1/V2, for one head_dim.
+template <typename T, int D>
 static const void *attn_kernel_ptr(int block_size, int group, bool v1)
 {
     const bool nt2 = group > 8;
-#define PA_PICK(BS, NT)                                                                           \
-    return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, BS, NT, true>)                    \
-              : reinterpret_cast<const void *>(&attn_kernel<T, BS, NT, false>)
-    if (block_size == 16) {
-        if (nt2) {
-            PA_PICK(16, 2);
-        }
-        PA_PICK(16, 1);
+#define PA_PICK(BS)                                                                               \
+    if (block_size == BS) {                                                                       \
+        if (nt2)                                                                                  \
+            return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 2, true>)           \
+                      : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 2, false>);         \
+        return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, true>)               \
+                  : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, false>);             \
     }
-    if (nt2) {
-        PA_PICK(32, 2);
-    }
-    PA_PICK(32, 1);
+    PA_PICK(16)
+    PA_PICK(32)
+    PA_PICK(64)
 #undef PA_PICK
+    return nullptr;
 }
 
 // Opts the kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory; returns that limit in *limit.
-template <typename T>
+template <typename T, int D>
 static cudaError_t attn_prepare(int block_size, int group, bool v1, int optin_bytes, size_t *limit)
 {
-    const void *fn = attn_kernel_ptr<T>(block_size, group, v1);
+    const void *fn = attn_kernel_ptr<T, D>(block_size, group, v1);
+    if (!fn)
+        return cudaErrorInvalidValue;
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, fn);
     if (e != cudaSuccess)
@@ -460,20 +467,23 @@ static cudaError_t attn_prepare(int block_size, int group, bool v1, int optin_by
 }
 
 // Resident CTAs per SM for a launch shape (0 on error).
-template <typename T>
-static int attn_occupancy_t(int block_size, int group, bool v1, int warps, size_t smem_bytes)
+template <typename T, int D>
+static int attn_occupancy(int block_size, int group, bool v1, int warps, size_t smem_bytes)
 {
+    const void *fn = attn_kernel_ptr<T, D>(block_size, group, v1);
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel_ptr<T>(block_size, group, v1),
-                                                      warps * 32, smem_bytes) != cudaSuccess)
+    if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, warps * 32, smem_bytes) !=
+                   cudaSuccess)
         return 0;
     return n;
 }
 
-template <typename T>
+template <typename T, int D>
 static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
 {
-    const void *fn = attn_kernel_ptr<T>(L.block_size, L.p.group, L.v1);
+    const void *fn = attn_kernel_ptr<T, D>(L.block_size, L.p.group, L.v1);
+    if (!fn)
+        return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
                     const_cast<AttnParams *>(&L.p)};
     cudaLaunchConfig_t cfg = {};
@@ -488,5 +498,14 @@ static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
     cfg.numAttrs = 1;
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
+
+// The table one translation unit exports for its (storage type, head_dim).
+#define PA_DEFINE_ATTN_OPS(T, NAME, D)                                                            \
+    const AttnOps *NAME()                                                                         \
+    {                                                                                             \
+        static const AttnOps ops = {&attn_prepare<T, D>, &attn_occupancy<T, D>,                   \
+                                    &attn_launch<T, D>};                                          \
+        return &ops;                                                                              \
+    }
 
 } // namespace pa

@@ -6,9 +6,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa_decode.h"
+
 namespace pa {
 
-constexpr int kHeadDim = 128;
 constexpr int kMaxGroup = 16;        // query heads per KV head
 constexpr int kMaxWarps = 8;         // warps per attention CTA
 constexpr int kMaxStages = 8;        // TMA ring stages per warp
@@ -16,7 +17,7 @@ constexpr int kMergeThreads = 128;   // phase-2 CTA size
 
 // Arguments of the attention kernel (phase 1 of V2, or V1).
 struct AttnParams {
-    const void *query;           // [S, H, 128]
+    const void *query;           // [S, H, D]
     const int32_t *block_tables; // [S, max_blocks]
     const int32_t *seq_lens;     // [S]
     int num_heads;
@@ -29,10 +30,10 @@ struct AttnParams {
     int part_blocks;             // V2: blocks per partition
     int stages;                  // TMA ring stages per warp
     int max_num_partitions;      // V2: partition capacity of the intermediates
-    float *tmp_output;           // V2: [S, H, NPcap, 128]
+    float *tmp_output;           // V2: [S, H, NPcap, D]
     float *exp_sums;             // V2: [S, H, NPcap]
     float *max_logits;           // V2: [S, H, NPcap]
-    void *out;                   // V1: [S, H, 128]
+    void *out;                   // V1: [S, H, D]
     int32_t *status;
 };
 
@@ -40,7 +41,8 @@ struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
-    int block_size;              // 16 or 32
+    int head_dim;                // 64, 128 or 256
+    int block_size;              // 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
     dim3 grid;
@@ -51,6 +53,7 @@ struct AttnLaunch {
 struct MergeParams {
     const int32_t *seq_lens;
     int num_heads;
+    int head_dim;
     int seq_len_cap;
     int partition_size;
     int max_num_partitions;
@@ -61,25 +64,45 @@ struct MergeParams {
     int32_t *status;
 };
 
-// Per-warp shared-memory ring bytes for one stage: K and V tiles, 2 halves of 128-byte lines.
-inline size_t stage_bytes(int block_size) { return static_cast<size_t>(block_size) * 512; }
-
-// Scratch one warp needs to hand its partial {m, l, o} to the CTA merge.
-inline size_t warp_scratch_bytes(int group)
+// Per-warp shared-memory ring bytes for one stage: a K tile and a V tile of
+// block_size rows x head_dim 16-bit values.
+inline size_t stage_bytes(int block_size, int head_dim)
 {
-    int heads = group <= 8 ? 8 : 16;
-    return static_cast<size_t>(heads) * (2 + 132) * 4;
+    return static_cast<size_t>(block_size) * head_dim * 4;
 }
 
-cudaError_t launch_attn_f16(const AttnLaunch &L, cudaStream_t stream);
-cudaError_t launch_attn_bf16(const AttnLaunch &L, cudaStream_t stream);
-cudaError_t attn_prepare_f16(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
-cudaError_t attn_prepare_bf16(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
+// Scratch one warp needs to hand its partial {m, l, o} to the CTA merge.
+inline size_t warp_scratch_bytes(int group, int head_dim)
+{
+    int heads = group <= 8 ? 8 : 16;
+    return static_cast<size_t>(heads) * (2 + head_dim + 4) * 4;
+}
+
+// Entry points of the attention kernels for one (storage type, head_dim).
+struct AttnOps {
+    cudaError_t (*prepare)(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
+    int (*occupancy)(int block_size, int group, bool v1, int warps, size_t smem_bytes);
+    cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
+};
+const AttnOps *attn_ops_f16_d64();
+const AttnOps *attn_ops_f16_d128();
+const AttnOps *attn_ops_f16_d256();
+const AttnOps *attn_ops_bf16_d64();
+const AttnOps *attn_ops_bf16_d128();
+const AttnOps *attn_ops_bf16_d256();
+
+inline const AttnOps *attn_ops(int dtype, int head_dim)
+{
+    if (dtype == PA_BF16)
+        return head_dim == 64 ? attn_ops_bf16_d64() : head_dim == 128 ? attn_ops_bf16_d128()
+                                                                       : attn_ops_bf16_d256();
+    return head_dim == 64 ? attn_ops_f16_d64() : head_dim == 128 ? attn_ops_f16_d128()
+                                                                  : attn_ops_f16_d256();
+}
+
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
                          cudaStream_t stream);
-int attn_occupancy(int dtype, int block_size, int group, bool v1, int warps, size_t smem_bytes);
-int attn_occupancy_f16(int block_size, int group, bool v1, int warps, size_t smem_bytes);
-int attn_occupancy_bf16(int block_size, int group, bool v1, int warps, size_t smem_bytes);
+
 cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns, cudaStream_t stream);
 
 } // namespace pa

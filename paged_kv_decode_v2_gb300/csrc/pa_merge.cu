@@ -6,8 +6,8 @@
 //     out        = sum_p (rescale_p / sum_q rescale_q) * tmp_output[p]
 // and the self-test kernel of the bounded wait.
 //
-// One CTA per (query head, sequence, slice of head_dim); the slice is the
-// whole head or a half, quarter or eighth of it when there are few (seq, head)
+// One CTA per (query head, sequence, slice of head_dim); the slice is at
+// most 128 dims, and smaller (down to 16) when there are few (seq, head)
 // pairs.  A group of lanes owns one partition at a time and reads the
 // slice as float4s (contiguous bytes); the groups of a CTA take partitions
 // round robin and their running states meet in shared memory.
@@ -16,12 +16,11 @@
 
 namespace pa {
 
-template <typename T, int DSPLIT>
+template <typename T, int DD>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p)
 {
     using E = Elem<T>;
-    constexpr int kDims = kHeadDim / DSPLIT;       // dims of head_dim this CTA owns
-    constexpr int kGroup = kDims / 4;              // lanes per partition (one float4 each)
+    constexpr int kGroup = DD / 4;                 // lanes per partition (one float4 each)
     constexpr int kSlots = kMergeThreads / kGroup; // partitions in flight per CTA
     __shared__ float s_m[kSlots];
     __shared__ float s_l[kSlots];
@@ -29,7 +28,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 
     const int h = blockIdx.x;
     const int b = blockIdx.y;
-    const int d0 = blockIdx.z * kDims;
+    const int D = p.head_dim;
+    const int d0 = blockIdx.z * DD;
     const int slot = threadIdx.x / kGroup; // partitions slot, slot + kSlots, ...
     const int c = threadIdx.x % kGroup;    // float4 column within the CTA's dims
 
@@ -41,15 +41,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
     const int np = (L + p.partition_size - 1) / p.partition_size;
     const size_t bh = (size_t)b * p.num_heads + h;
-    T *out = static_cast<T *>(p.out) + bh * kHeadDim + d0;
+    T *out = static_cast<T *>(p.out) + bh * D + d0;
     if (np == 0) {
-        if (threadIdx.x < kDims)
+        if (threadIdx.x < DD)
             out[threadIdx.x] = E::from_float(0.f);
         return;
     }
     const float *ml = p.max_logits + bh * p.max_num_partitions;
     const float *es = p.exp_sums + bh * p.max_num_partitions;
-    const float4 *tmp = reinterpret_cast<const float4 *>(p.tmp_output + bh * p.max_num_partitions * kHeadDim + d0);
+    const float4 *tmp = reinterpret_cast<const float4 *>(p.tmp_output + bh * p.max_num_partitions * D + d0);
+    const int row4 = D / 4; // float4s between partitions
 
     // Phase 1's results are visible only after this point.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -63,7 +64,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     for (int i = slot; i < np; i += kSlots) {
         const float mp = __ldg(ml + i);
         const float lp = __ldg(es + i);
-        const float4 v = __ldg(tmp + (size_t)i * (kHeadDim / 4) + c);
+        const float4 v = __ldg(tmp + (size_t)i * row4 + c);
         const float mn = fmaxf(m, mp);
         const float a = fast_exp2((m - mn) * kLog2e); // 0 while m is -inf
         const float w = fast_exp2((mp - mn) * kLog2e) * lp;
@@ -81,7 +82,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     }
     __syncthreads();
 
-    if (threadIdx.x < kDims) {
+    if (threadIdx.x < DD) {
         const int d = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
@@ -100,28 +101,28 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
 }
 
 template <typename T>
-static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dsplit, const MergeParams &p)
+static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dd, const MergeParams &p)
 {
-    if (dsplit == 8)
-        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 8>, p);
-    if (dsplit == 4)
-        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 4>, p);
-    if (dsplit == 2)
-        return cudaLaunchKernelEx(&cfg, merge_kernel<T, 2>, p);
-    return cudaLaunchKernelEx(&cfg, merge_kernel<T, 1>, p);
+    switch (dd) {
+    case 16: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 16>, p);
+    case 32: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 32>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 64>, p);
+    default: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 128>, p);
+    }
 }
 
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
                          cudaStream_t stream)
 {
-    // Split head_dim over 1, 2, 4 or 8 CTAs so that the grid has at least
-    // about two CTAs per SM; a finer split only adds CTAs of very little work.
+    // A CTA owns at most 128 dims of head_dim; split further (down to 16
+    // dims) while the grid has fewer than about two CTAs per SM -- a finer
+    // split only adds CTAs of very little work.
     const long long pairs = (long long)p.num_heads * num_seqs;
-    int dsplit = 1;
-    while (dsplit < 8 && pairs * dsplit < 2LL * num_sms)
-        dsplit *= 2;
+    int dd = p.head_dim < 128 ? p.head_dim : 128;
+    while (dd > 16 && pairs * (p.head_dim / dd) < 2LL * num_sms)
+        dd /= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_heads, num_seqs, dsplit);
+    cfg.gridDim = dim3(p.num_heads, num_seqs, p.head_dim / dd);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -133,8 +134,8 @@ cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (dtype == PA_BF16)
-        return launch_merge_t<__nv_bfloat16>(cfg, dsplit, p);
-    return launch_merge_t<__half>(cfg, dsplit, p);
+        return launch_merge_t<__nv_bfloat16>(cfg, dd, p);
+    return launch_merge_t<__half>(cfg, dd, p);
 }
 
 // One warp waits on a barrier that nothing completes; the bounded wait must

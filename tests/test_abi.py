@@ -76,7 +76,9 @@ def _v2(lib, **kw):
     (dict(num_heads=6, num_kv_heads=4), 1),
     (dict(dtype=2), 1),
     (dict(scale=float("nan")), 1),
-    (dict(head_dim=64), 2),
+    (dict(head_dim=96), 2),
+    (dict(head_dim=512), 2),
+    (dict(block_size=48), 2),
     (dict(block_size=8), 2),
     (dict(num_heads=64, num_kv_heads=2), 2),
     (dict(partition_size=500), 1),
@@ -91,7 +93,7 @@ def test_invalid_arguments_fail_before_launch(cuda_lib, kw, code):
 
 def test_invalid_arguments_v1_and_dispatch(cuda_lib):
     lib = cuda_lib.load()
-    args = [FAKE] * 5 + [1, 8, 2, 64, 128, 16, 63, 0, 0.088]
+    args = [FAKE] * 5 + [1, 8, 2, 80, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_v1(*args, 0, FAKE, None, None) == 2
     args = [FAKE] * 5 + [1, 8, 2, 128, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_v1(*args, 0, None, None, None) == 1

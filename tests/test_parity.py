@@ -60,6 +60,41 @@ def test_fuzz_grid(dtype, bs, G, P):
     full_check(wl.make_inputs(w, device="cuda"), P)
 
 
+@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("G", [1, 8, 16])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_fuzz_head_dims(D, bs, G, dtype):
+    P = 128
+    lens = (1, bs - 1, bs + 1, P - 1, P + 1, 3 * P + bs + 3)
+    w = wl.Workload("fuzz_d", len(lens), 2 * G, 2, D, bs, P, dtype, "list", seq_lens=lens,
+                    seed=2000 + D + 7 * G + bs + dtype)
+    full_check(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
+@pytest.mark.parametrize("P", [128, 512])
+def test_fuzz_block_size_64(dtype, G, P):
+    lens = (1, 63, 64, 65, P - 1, P + 1, 2 * P + 67)
+    w = wl.Workload("fuzz_bs64", len(lens), 2 * G, 2, 128, 64, P, dtype, "list", seq_lens=lens,
+                    seed=3000 + 7 * G + P + dtype)
+    full_check(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("D", [64, 256])
+@pytest.mark.parametrize("warps,stages", [(1, 1), (2, 2), (8, 1), (3, 3)])
+def test_launch_shapes_other_head_dims(cuda_lib, D, warps, stages):
+    w = wl.Workload("shapes_d", 3, 16, 2, D, 32, 256, wl.BF16, "list", seq_lens=(700, 2049, 5),
+                    seed=56 + D)
+    inp = wl.make_inputs(w, device="cuda")
+    cuda_lib.pa_set_launch_config(warps, stages)
+    try:
+        full_check(inp, 256, entries=("v2", "v1"))
+    finally:
+        cuda_lib.pa_set_launch_config(0, 0)
+
+
 @pytest.mark.parametrize("warps,stages", [(1, 1), (1, 2), (2, 1), (2, 4), (8, 2), (3, 3), (4, 8)])
 def test_launch_shapes_do_not_change_results(cuda_lib, warps, stages):
     w = wl.Workload("shapes", 4, 16, 2, 128, 16, 256, wl.BF16, "list",
