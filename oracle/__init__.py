@@ -64,17 +64,25 @@ def _ptr(a: np.ndarray):
 
 
 class Problem:
-    """One decode problem in the paged layout (numpy views, no copies of the caches)."""
+    """One decode problem in the paged layout (numpy views, no copies of the caches).
+
+    query is [S, H, D] (one new token per sequence) or [S, Q, H, D] (Q new
+    tokens per sequence, each attending to its causal prefix).
+    """
 
     def __init__(self, query, key_cache, value_cache, block_tables, seq_lens, scale, dtype):
-        self.query = _u16(query)            # [S, H, D]
+        self.query = _u16(query)            # [S, H, D] or [S, Q, H, D]
         self.key_cache = _u16(key_cache)    # [num_blocks, KV, bs, D]
         self.value_cache = _u16(value_cache)
         self.block_tables = _i32(block_tables)  # [S, max_blocks]
         self.seq_lens = _i32(seq_lens)          # [S]
         self.scale = float(scale)
         self.dtype = int(dtype)
-        S, H, D = self.query.shape
+        if self.query.ndim == 4:
+            S, Q, H, D = self.query.shape
+        else:
+            (S, H, D), Q = self.query.shape, 1
+        self.Q = Q
         nb, KV, bs, D2 = self.key_cache.shape
         if D2 != D or self.value_cache.shape != self.key_cache.shape:
             raise ValueError("cache / query shape mismatch")
@@ -90,13 +98,17 @@ class Problem:
 
     def _args(self):
         return [_ptr(self.query), _ptr(self.key_cache), _ptr(self.value_cache),
-                _ptr(self.block_tables), _ptr(self.seq_lens), self.S, self.H, self.KV, self.D,
-                self.num_blocks, self.bs, self.max_blocks, self.scale, self.dtype]
+                _ptr(self.block_tables), _ptr(self.seq_lens), self.S, self.Q, self.H, self.KV,
+                self.D, self.num_blocks, self.bs, self.max_blocks, self.scale, self.dtype]
+
+    def out_shape(self):
+        return (self.S, self.Q, self.H, self.D) if self.query.ndim == 4 else (self.S, self.H, self.D)
 
 
 def _pairs(problem: Problem, pairs):
+    """pairs are (row, head) with row = b * Q + i (row = b when Q = 1)."""
     if pairs is None:
-        return None, problem.S * problem.H
+        return None, problem.S * problem.Q * problem.H
     arr = _i32(pairs).reshape(-1, 2)
     return arr, arr.shape[0]
 
@@ -109,11 +121,11 @@ class OracleLib:
         P = ctypes.c_void_p
         I = ctypes.c_int
         D = ctypes.c_double
-        lib.pa_oracle_decode.restype = I
-        lib.pa_oracle_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, I, P, I, P, I]
-        lib.pa_oracle_partition_stats.restype = I
-        lib.pa_oracle_partition_stats.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, D, I, I, P,
-                                                  I, I, P, P, P, P, I]
+        lib.pa_oracle_decode_mq.restype = I
+        lib.pa_oracle_decode_mq.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, P, I, P, I]
+        lib.pa_oracle_partition_stats_mq.restype = I
+        lib.pa_oracle_partition_stats_mq.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, D, I,
+                                                     I, P, I, I, P, P, P, P, I]
         lib.pa_oracle_merge.restype = I
         lib.pa_oracle_merge.argtypes = [P, P, P, I, I, P]
         lib.pa_oracle_decode_scalar.restype = D
@@ -122,14 +134,14 @@ class OracleLib:
         self.path = path
 
     def decode(self, problem: Problem, pairs=None, num_threads: int = 0) -> np.ndarray:
-        """Unpartitioned softmax decode.  Returns [S, H, D] (pairs=None) or [n, D] doubles."""
+        """Unpartitioned softmax decode.  Returns the query's shape (pairs=None) or [n, D] doubles."""
         arr, n = _pairs(problem, pairs)
         out = np.empty((n, problem.D), dtype=np.float64)
-        rc = self.lib.pa_oracle_decode(*problem._args(), None if arr is None else _ptr(arr), n,
-                                       _ptr(out), int(num_threads))
+        rc = self.lib.pa_oracle_decode_mq(*problem._args(), None if arr is None else _ptr(arr), n,
+                                          _ptr(out), int(num_threads))
         if rc:
             raise RuntimeError(f"pa_oracle_decode failed with code {rc}")
-        return out.reshape(problem.S, problem.H, problem.D) if arr is None else out
+        return out.reshape(problem.out_shape()) if arr is None else out
 
     def partition_stats(self, problem: Problem, partition_size: int, pairs=None,
                         max_partitions=None, num_threads: int = 0):
@@ -141,7 +153,7 @@ class OracleLib:
         m = np.full((n, max_partitions), np.nan)
         l = np.full((n, max_partitions), np.nan)
         num = np.zeros(n, dtype=np.int32)
-        rc = self.lib.pa_oracle_partition_stats(*problem._args(), int(partition_size),
+        rc = self.lib.pa_oracle_partition_stats_mq(*problem._args(), int(partition_size),
                                                 None if arr is None else _ptr(arr), n,
                                                 int(max_partitions), _ptr(o), _ptr(m), _ptr(l),
                                                 _ptr(num), int(num_threads))

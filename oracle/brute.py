@@ -17,7 +17,18 @@ from __future__ import annotations
 import math
 
 
-def decode(query, key_cache, value_cache, block_tables, seq_lens, scale):
+def decode(query, key_cache, value_cache, block_tables, seq_lens, scale, q_len=None):
+    """query [S][H][D], or [S][Q][H][D] with q_len = Q (query i sees t <= L - Q + i)."""
+    if q_len is not None:
+        rows = []
+        for b in range(len(query)):
+            per_i = []
+            for i in range(q_len):
+                visible = max(0, min(int(seq_lens[b]), int(seq_lens[b]) - q_len + i + 1))
+                per_i.append(decode([query[b][i]], key_cache, value_cache, [block_tables[b]],
+                                    [visible], scale)[0])
+            rows.append(per_i)
+        return rows
     S = len(query)
     H = len(query[0])
     D = len(query[0][0])

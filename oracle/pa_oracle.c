@@ -31,6 +31,16 @@
  * oracle_decode() writes exactly that out.  Subtracting max(s) inside the
  * exponent is an exact rewrite of softmax that only avoids overflow.
  *
+ * Several new tokens per sequence (multi-query decode, q_len = Q >= 1): the
+ * query is [S, Q, H, D] and query i of sequence b sits at position
+ * L - Q + i, so it attends to the causal prefix t <= L - Q + i ("the
+ * [kv_h, gqa, q_len, tile] batching" of the "paged_attn.py" commit 490ff98
+ * online-softmax paragraph; the pages leave the mask implicit, and the
+ * causal prefix is the reading taken).  A query that sees no token has a
+ * zero output; a partition holding none of its visible tokens has
+ * m_p = -inf, l_p = 0, o_p = 0 and contributes nothing to the merge.
+ * Q = 1 is the single-query decode above.
+ *
  * Storage types: query / key_cache / value_cache arrive as raw 16-bit
  * patterns (IEEE binary16 or bfloat16) and are decoded to double exactly by
  * this file's own bit decoding.  All arithmetic is in double.
@@ -90,7 +100,7 @@ double pa_oracle_decode_scalar(uint16_t bits, int dtype) { return decode16(bits,
 /* ---------- problem description ---------- */
 
 typedef struct {
-    const uint16_t *query;       /* [S, H, D] */
+    const uint16_t *query;       /* [S, Q, H, D] */
     const uint16_t *key_cache;   /* [num_blocks, KV, bs, D] */
     const uint16_t *value_cache; /* [num_blocks, KV, bs, D] */
     const int32_t *block_tables; /* [S, max_blocks] */
@@ -98,6 +108,7 @@ typedef struct {
     int S, H, KV, D, num_blocks, bs, max_blocks;
     double scale;
     int dtype;
+    int Q; /* new tokens per sequence */
 } problem_t;
 
 static int check_problem(const problem_t *p)
@@ -107,7 +118,7 @@ static int check_problem(const problem_t *p)
     if (p->S <= 0 || p->H <= 0 || p->KV <= 0 || p->D <= 0 || p->bs <= 0 || p->num_blocks <= 0 ||
         p->max_blocks <= 0)
         return ORACLE_EINVAL;
-    if (p->H % p->KV != 0)
+    if (p->H % p->KV != 0 || p->Q < 1)
         return ORACLE_EINVAL;
     if (p->dtype != ORACLE_F16 && p->dtype != ORACLE_BF16)
         return ORACLE_EINVAL;
@@ -142,9 +153,10 @@ static int logits(const problem_t *p, int b, int h, int t0, int t1, const double
     return ORACLE_OK;
 }
 
-static void load_query(const problem_t *p, int b, int h, double *q)
+/* Query row (sequence b, new token i) = r = b * Q + i. */
+static void load_query(const problem_t *p, int r, int h, double *q)
 {
-    const uint16_t *qrow = p->query + ((int64_t)b * p->H + h) * p->D;
+    const uint16_t *qrow = p->query + ((int64_t)r * p->H + h) * p->D;
     for (int d = 0; d < p->D; ++d)
         q[d] = decode16(qrow[d], p->dtype);
 }
@@ -189,7 +201,7 @@ static int softmax_v(const problem_t *p, int b, int h, int t0, int t1, const dou
 
 typedef struct {
     const problem_t *p;
-    const int32_t *pairs; /* [n, 2] (b, h) or NULL for all S*H in order */
+    const int32_t *pairs; /* [n, 2] (r, h), r = b * Q + i, or NULL for all S*Q*H in order */
     int n;
     int partition_size;   /* 0: full decode; >0: partition statistics */
     int max_partitions;   /* capacity of the per-pair partition arrays */
@@ -202,13 +214,13 @@ typedef struct {
     int rc;
 } job_t;
 
-static void pair_at(const job_t *j, int i, int *b, int *h)
+static void pair_at(const job_t *j, int i, int *r, int *h)
 {
     if (j->pairs) {
-        *b = j->pairs[2 * i];
+        *r = j->pairs[2 * i];
         *h = j->pairs[2 * i + 1];
     } else {
-        *b = i / j->p->H;
+        *r = i / j->p->H;
         *h = i % j->p->H;
     }
 }
@@ -225,23 +237,30 @@ static void *worker(void *arg)
         goto done;
     }
     for (int i = j->tid; i < j->n; i += j->nthreads) {
-        int b, h;
-        pair_at(j, i, &b, &h);
-        if (b < 0 || b >= p->S || h < 0 || h >= p->H) {
+        int r, h;
+        pair_at(j, i, &r, &h);
+        if (r < 0 || r >= p->S * p->Q || h < 0 || h >= p->H) {
             j->rc = ORACLE_EINVAL;
             goto done;
         }
+        int b = r / p->Q;
         int L = p->seq_lens[b];
-        load_query(p, b, h, q);
+        /* tokens this query sees: t < visible, the causal prefix up to L - Q + i */
+        int visible = L - p->Q + r % p->Q + 1;
+        if (visible < 0)
+            visible = 0;
+        if (visible > L)
+            visible = L;
+        load_query(p, r, h, q);
         if (j->partition_size == 0) {
             double *dst = j->out + (int64_t)i * p->D;
-            if (L == 0) { /* no keys: defined as a zero output */
+            if (visible == 0) { /* no keys: defined as a zero output */
                 for (int d = 0; d < p->D; ++d)
                     dst[d] = 0.0;
                 continue;
             }
             double m, l;
-            int rc = softmax_v(p, b, h, 0, L, q, s, dst, &m, &l);
+            int rc = softmax_v(p, b, h, 0, visible, q, s, dst, &m, &l);
             if (rc) {
                 j->rc = rc;
                 goto done;
@@ -257,7 +276,16 @@ static void *worker(void *arg)
             for (int part = 0; part < np; ++part) {
                 int t0 = part * P;
                 int t1 = t0 + P < L ? t0 + P : L;
+                if (t1 > visible)
+                    t1 = visible;
                 int64_t slot = (int64_t)i * j->max_partitions + part;
+                if (t1 <= t0) { /* none of this partition's tokens is visible */
+                    j->m_p[slot] = -INFINITY;
+                    j->l_p[slot] = 0.0;
+                    for (int d = 0; d < p->D; ++d)
+                        j->o_p[slot * p->D + d] = 0.0;
+                    continue;
+                }
                 int rc = softmax_v(p, b, h, t0, t1, q, s, j->o_p + slot * p->D, &j->m_p[slot],
                                    &j->l_p[slot]);
                 if (rc) {
@@ -322,18 +350,20 @@ static int run_jobs(job_t *proto, int nthreads)
  * NULL for every (b, h) in row-major order (num_pairs must then be S*H).
  * out: [num_pairs, D] doubles.  Returns 0 on success.
  */
-int pa_oracle_decode(const uint16_t *query, const uint16_t *key_cache, const uint16_t *value_cache,
-                     const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
-                     int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
-                     int max_blocks_per_seq, double scale, int dtype, const int32_t *pairs,
-                     int num_pairs, double *out, int num_threads)
+int pa_oracle_decode_mq(const uint16_t *query, const uint16_t *key_cache,
+                        const uint16_t *value_cache, const int32_t *block_tables,
+                        const int32_t *seq_lens, int num_seqs, int q_len, int num_heads,
+                        int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                        int max_blocks_per_seq, double scale, int dtype, const int32_t *pairs,
+                        int num_pairs, double *out, int num_threads)
 {
     problem_t p = {query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                   num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, scale, dtype};
+                   num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, scale, dtype,
+                   q_len};
     int rc = check_problem(&p);
     if (rc)
         return rc;
-    if (!out || num_pairs < 0 || (!pairs && num_pairs != num_seqs * num_heads))
+    if (!out || num_pairs < 0 || (!pairs && num_pairs != num_seqs * q_len * num_heads))
         return ORACLE_EINVAL;
     job_t j;
     memset(&j, 0, sizeof j);
@@ -346,6 +376,18 @@ int pa_oracle_decode(const uint16_t *query, const uint16_t *key_cache, const uin
     return run_jobs(&j, num_threads);
 }
 
+int pa_oracle_decode(const uint16_t *query, const uint16_t *key_cache, const uint16_t *value_cache,
+                     const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                     int max_blocks_per_seq, double scale, int dtype, const int32_t *pairs,
+                     int num_pairs, double *out, int num_threads)
+{
+    return pa_oracle_decode_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, 1,
+                               num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, scale, dtype, pairs, num_pairs, out,
+                               num_threads);
+}
+
 /*
  * Phase 1 of the pages' V2, per (seq, head, partition): for partition
  * part = 0 .. ceil(L/P)-1 covering tokens [part*P, min(L, (part+1)*P)),
@@ -353,21 +395,23 @@ int pa_oracle_decode(const uint16_t *query, const uint16_t *key_cache, const uin
  * Arrays are per pair with capacity max_partitions; num_p[i] receives the
  * partition count ceil(L/P) of pair i.  Entries past num_p[i] are untouched.
  */
-int pa_oracle_partition_stats(const uint16_t *query, const uint16_t *key_cache,
-                              const uint16_t *value_cache, const int32_t *block_tables,
-                              const int32_t *seq_lens, int num_seqs, int num_heads,
-                              int num_kv_heads, int head_dim, int num_blocks, int block_size,
-                              int max_blocks_per_seq, double scale, int dtype, int partition_size,
-                              const int32_t *pairs, int num_pairs, int max_partitions, double *o_p,
-                              double *m_p, double *l_p, int32_t *num_p, int num_threads)
+int pa_oracle_partition_stats_mq(const uint16_t *query, const uint16_t *key_cache,
+                                 const uint16_t *value_cache, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int num_seqs, int q_len, int num_heads,
+                                 int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                                 int max_blocks_per_seq, double scale, int dtype,
+                                 int partition_size, const int32_t *pairs, int num_pairs,
+                                 int max_partitions, double *o_p, double *m_p, double *l_p,
+                                 int32_t *num_p, int num_threads)
 {
     problem_t p = {query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                   num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, scale, dtype};
+                   num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, scale, dtype,
+                   q_len};
     int rc = check_problem(&p);
     if (rc)
         return rc;
     if (partition_size <= 0 || max_partitions <= 0 || !o_p || !m_p || !l_p || !num_p ||
-        num_pairs < 0 || (!pairs && num_pairs != num_seqs * num_heads))
+        num_pairs < 0 || (!pairs && num_pairs != num_seqs * q_len * num_heads))
         return ORACLE_EINVAL;
     job_t j;
     memset(&j, 0, sizeof j);
@@ -385,6 +429,21 @@ int pa_oracle_partition_stats(const uint16_t *query, const uint16_t *key_cache,
     return run_jobs(&j, num_threads);
 }
 
+int pa_oracle_partition_stats(const uint16_t *query, const uint16_t *key_cache,
+                              const uint16_t *value_cache, const int32_t *block_tables,
+                              const int32_t *seq_lens, int num_seqs, int num_heads,
+                              int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                              int max_blocks_per_seq, double scale, int dtype, int partition_size,
+                              const int32_t *pairs, int num_pairs, int max_partitions, double *o_p,
+                              double *m_p, double *l_p, int32_t *num_p, int num_threads)
+{
+    return pa_oracle_partition_stats_mq(query, key_cache, value_cache, block_tables, seq_lens,
+                                        num_seqs, 1, num_heads, num_kv_heads, head_dim, num_blocks,
+                                        block_size, max_blocks_per_seq, scale, dtype,
+                                        partition_size, pairs, num_pairs, max_partitions, o_p, m_p,
+                                        l_p, num_p, num_threads);
+}
+
 /*
  * Phase 2 of the pages' V2 for one (seq, head): the log-sum-exp merge of
  * num_partitions partial results o_p [num_partitions, D], m_p, l_p:
@@ -392,7 +451,8 @@ int pa_oracle_partition_stats(const uint16_t *query, const uint16_t *key_cache,
  *   rescale_p  = exp(m_p - global_max) * l_p
  *   total_sum  = sum_p rescale_p
  *   out        = sum_p (rescale_p / total_sum) * o_p
- * num_partitions == 0 gives a zero output.
+ * num_partitions == 0, or partitions that are all empty (l_p = 0), give a
+ * zero output; an empty partition (m_p = -inf, l_p = 0) adds nothing.
  */
 int pa_oracle_merge(const double *o_p, const double *m_p, const double *l_p, int num_partitions,
                     int head_dim, double *out)
@@ -407,10 +467,14 @@ int pa_oracle_merge(const double *o_p, const double *m_p, const double *l_p, int
     for (int i = 0; i < num_partitions; ++i)
         if (m_p[i] > global_max)
             global_max = m_p[i];
+    if (global_max == -INFINITY)
+        return ORACLE_OK;
     double total_sum = 0.0;
     for (int i = 0; i < num_partitions; ++i)
         total_sum += exp(m_p[i] - global_max) * l_p[i];
     for (int i = 0; i < num_partitions; ++i) {
+        if (l_p[i] == 0.0)
+            continue;
         double weight = exp(m_p[i] - global_max) * l_p[i] / total_sum;
         for (int d = 0; d < head_dim; ++d)
             out[d] += weight * o_p[(int64_t)i * head_dim + d];

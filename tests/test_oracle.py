@@ -317,6 +317,77 @@ def test_pairs_subset_matches_full():
         assert np.array_equal(sub[i], full[b, h])
 
 
+# ---------------------------------------------------------------- several new tokens (q_len > 1)
+
+def mq_workload(q_len, lens, H=8, KV=2, D=32, bs=16, P=64, dtype=wl.BF16, seed=11):
+    return wl.Workload("mq", len(lens), H, KV, D, bs, P, dtype, "list", seq_lens=tuple(lens),
+                       q_len=q_len, seed=seed)
+
+
+def mq_torch_reference(inp):
+    """Dense gather + torch.softmax(float64) over each query's causal prefix t <= L - Q + i."""
+    w = inp.workload
+    Q, G = w.q_len, w.group_size
+    S = w.num_seqs
+    out = np.zeros(tuple(inp.query.shape), dtype=np.float64)
+    for b in range(S):
+        L = int(inp.seq_lens[b])
+        if L == 0:
+            continue
+        k, v = dense_kv(inp, b)
+        for i in range(Q):
+            vis = min(L, max(0, L - Q + i + 1))
+            if vis == 0:
+                continue
+            for h in range(w.num_heads):
+                s = (k[:vis, h // G].to(torch.float64) @ inp.query[b, i, h].to(torch.float64)) * w.scale
+                out[b, i, h] = (torch.softmax(s, 0) @ v[:vis, h // G].to(torch.float64)).numpy()
+    return out
+
+
+def test_mq_single_token_is_the_single_query_decode():
+    w1 = small(seq_lens=(5, 300, 64))
+    inp1 = wl.make_inputs(w1)
+    arrs = wl.to_oracle_arrays(inp1)
+    single = oracle.decode(oracle.Problem.from_arrays(arrs))
+    arrs4 = dict(arrs, query=arrs["query"][:, None])  # [S, 1, H, D]
+    multi = oracle.decode(oracle.Problem.from_arrays(arrs4))
+    assert multi.shape == (3, 1, 8, 32)
+    assert np.array_equal(multi[:, 0], single)
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 7])
+def test_mq_matches_causal_prefix_softmax(q_len):
+    inp = wl.make_inputs(mq_workload(q_len, (1, 2, q_len, 17, 200)))
+    out = oracle.decode(problem_of(inp))
+    np.testing.assert_allclose(out, mq_torch_reference(inp), rtol=1e-12, atol=1e-13)
+    L0 = 1  # sequence 0 is shorter than q_len: its first queries see nothing
+    assert np.all(out[0, : q_len - L0] == 0.0)
+
+
+@pytest.mark.parametrize("P", [16, 64, 48])
+def test_mq_partition_then_merge_equals_unpartitioned(P):
+    inp = wl.make_inputs(mq_workload(4, (3, 63, 64, 65, 129, 200)))
+    prob = problem_of(inp)
+    full = oracle.decode(prob).reshape(-1, prob.D)
+    o, m, l, num = oracle.partition_stats(prob, P)
+    for idx in range(full.shape[0]):
+        n = int(num[idx])
+        merged = oracle.merge(o[idx, :n], m[idx, :n], l[idx, :n])
+        np.testing.assert_allclose(merged, full[idx], rtol=1e-12, atol=1e-13)
+    # a partition holding none of a query's visible tokens is empty, not NaN
+    assert np.isfinite(o[~np.isnan(o)]).all()
+    assert (l[~np.isnan(l)] >= 0).all()
+
+
+def test_mq_matches_pure_python_brute_force():
+    inp = wl.make_inputs(mq_workload(3, (7, 2), H=4, KV=2, D=8, bs=4))
+    out = oracle.decode(problem_of(inp))
+    ref = brute.decode(decoded(inp.query), decoded(inp.key_cache), decoded(inp.value_cache),
+                       inp.block_tables.numpy(), inp.seq_lens.numpy(), inp.workload.scale, q_len=3)
+    np.testing.assert_allclose(out, np.array(ref), rtol=1e-13, atol=1e-14)
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 MUTANTS = {
@@ -334,6 +405,10 @@ MUTANTS = {
     "exp_sign": ("double w = exp(s[t - t0] - m);", "double w = exp(m - s[t - t0]);"),
     # binary16 exponent bias off by one
     "f16_bias": ("expo - 25", "expo - 24"),
+    # causal limit of a new token off by one
+    "causal_off_by_one": ("int visible = L - p->Q + r % p->Q + 1;", "int visible = L - p->Q + r % p->Q;"),
+    # query row of new token i taken from the wrong position
+    "mq_row": ("int b = r / p->Q;\n", "int b = r % p->S;\n"),
 }
 
 
@@ -375,6 +450,11 @@ def _pins_pass(lib: "oracle.OracleLib") -> bool:
             merged = lib.merge(o[i, : num[i]], m[i, : num[i]], l[i, : num[i]])
             if not np.allclose(merged, out[b, h], rtol=1e-12, atol=1e-13):
                 return False
+        # several new tokens: causal prefix softmax
+        inp = wl.make_inputs(mq_workload(3, (2, 40, 9)))
+        mq = lib.decode(problem_of(inp))
+        if not np.allclose(mq, mq_torch_reference(inp), rtol=1e-12, atol=1e-13):
+            return False
         return True
     except RuntimeError:
         return False

@@ -50,6 +50,7 @@ class Workload:
     pool_blocks: int = 0           # ... unless a fixed pool size is given
     outlier_frac: float = 0.0      # fraction of K channels scaled by outlier_scale
     outlier_scale: float = 1.0
+    q_len: int = 1                 # new tokens per sequence (query [S, q_len, H, D] when > 1)
     seed: int = 20261202
 
     @property
@@ -104,7 +105,7 @@ def blocks_for(seq_len: int, block_size: int) -> int:
 @dataclasses.dataclass
 class Inputs:
     workload: Workload
-    query: torch.Tensor          # [S, H, D] dtype
+    query: torch.Tensor          # [S, H, D] (or [S, Q, H, D] for q_len Q > 1) dtype
     key_cache: torch.Tensor      # [num_blocks, KV, bs, D] dtype
     value_cache: torch.Tensor    # [num_blocks, KV, bs, D] dtype
     block_tables: torch.Tensor   # [S, max_blocks] int32 (-1 padding)
@@ -169,7 +170,7 @@ def make_inputs(w: Workload, device="cpu", seq_lens: Optional[Sequence[int]] = N
     gdev = torch.Generator(device=device).manual_seed(w.seed + 1)
     dt = TORCH_DTYPE[w.dtype]
     H, KV, D = w.num_heads, w.num_kv_heads, w.head_dim
-    query = _randn((S, H, D), gdev, device, dt)
+    query = _randn((S, H, D) if w.q_len == 1 else (S, w.q_len, H, D), gdev, device, dt)
     if outliers:
         k32 = torch.randn((pool, KV, bs, D), generator=gdev, device=device, dtype=torch.float32)
         idx = torch.tensor(outliers, device=device)
