@@ -49,7 +49,8 @@
  *
  * Supported shapes: head_dim 64, 128 or 256; block_size 16, 32 or 64;
  * partition_size a positive multiple of block_size; G = num_heads /
- * num_kv_heads an integer in [1, 16].  Other shapes return
+ * num_kv_heads an integer in [1, 64]; q_len in [1, 64] with num_seqs *
+ * q_len <= 65535 (the _mq entry points).  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned
  * (they are read with the Tensor Memory Accelerator); query and out 4-byte
  * aligned.
@@ -166,6 +167,39 @@ PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_he
                                const float *tmp_output, const float *exp_sums,
                                const float *max_logits, int max_num_partitions, void *out,
                                int32_t *status, pa_stream_t stream);
+
+/*
+ * Several new tokens per sequence (multi-query decode, e.g. checking q_len
+ * speculated tokens at once).  The pages batch [kv_h, gqa, q_len, tile] in
+ * the "paged_attn.py" commit 490ff98 online-softmax paragraph; the causal
+ * mask they leave implicit is read as: new token i of sequence b sits at
+ * position L - q_len + i, where L = seq_lens[b] already counts the q_len new
+ * tokens, and attends to keys t <= L - q_len + i.  A new token that sees no
+ * key (L - q_len + i < 0) gets a zero output row.
+ *   query       [num_seqs, q_len, num_heads, head_dim]   dtype
+ *   out         [num_seqs, q_len, num_heads, head_dim]   dtype
+ *   tmp_output  [num_seqs, q_len, num_heads, max_num_partitions, head_dim]
+ *   exp_sums, max_logits  [num_seqs, q_len, num_heads, max_num_partitions]
+ * A partition holding none of the tokens a query sees is written as
+ * max_logits = -inf, exp_sums = 0, tmp_output = 0 and adds nothing to the
+ * merge.  The K/V cache is read once per call for all q_len * G query rows
+ * of a KV head; beyond 16 rows the rows are split over CTAs that run side
+ * by side, so their reads meet in L2.  q_len = 1 is pa_decode_v2 / _v1.
+ */
+PA_API int pa_decode_v2_mq(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int q_len, int num_heads, int num_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int max_seq_len_hint, float scale, int partition_size, int dtype,
+                           void *out, float *tmp_output, float *exp_sums, float *max_logits,
+                           int max_num_partitions, int32_t *status, pa_stream_t stream);
+
+PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int q_len, int num_heads, int num_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int max_seq_len_hint, float scale, int dtype, void *out,
+                           int32_t *status, pa_stream_t stream);
 
 /*
  * Single-pass decode: one CTA per (sequence, KV head) walks all blocks with

@@ -61,6 +61,11 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_v2_phase2.restype = I
     lib.pa_decode_v1.argtypes = attn + [I, P, P, P]
     lib.pa_decode_v1.restype = I
+    attn_mq = [P, P, P, P, P, I, I, I, I, I, I, I, I, I, F]
+    lib.pa_decode_v2_mq.argtypes = attn_mq + [I, I, P, P, P, P, I, P, P]
+    lib.pa_decode_v2_mq.restype = I
+    lib.pa_decode_v1_mq.argtypes = attn_mq + [I, P, P, P]
+    lib.pa_decode_v1_mq.restype = I
     lib.pa_decode.argtypes = attn + [I, I, P, P, P, P, I, P, P]
     lib.pa_decode.restype = I
     lib.pa_decode_choose.argtypes = [I, I, I, I]
@@ -112,6 +117,16 @@ def _shape_args(query, key_cache, value_cache, block_tables, seq_lens, max_seq_l
             S, H, KV, D, nb, bs, block_tables.shape[1], int(max_seq_len_hint), float(scale)]
 
 
+def _shape_args_mq(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint, scale):
+    """Arguments of the _mq entry points: query [S, Q, H, D]."""
+    if query.dim() != 4:
+        raise ValueError("query must be [num_seqs, q_len, num_heads, head_dim]")
+    S, Q, H, D = query.shape
+    a = _shape_args(query.view(S, Q * H, D), key_cache, value_cache, block_tables, seq_lens,
+                    max_seq_len_hint, scale)
+    return a[:5] + [S, Q, H] + a[7:]
+
+
 def num_partitions(max_seq_len: int, partition_size: int) -> int:
     return load().pa_v2_num_partitions(int(max_seq_len), int(partition_size))
 
@@ -121,11 +136,14 @@ def workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_num_partit
 
 
 def alloc_workspace(num_seqs: int, num_heads: int, head_dim: int, max_num_partitions: int,
-                    device="cuda"):
-    """Allocate (tmp_output, exp_sums, max_logits) once, to be reused across calls."""
-    tmp = torch.empty((num_seqs, num_heads, max_num_partitions, head_dim), dtype=torch.float32,
-                      device=device)
-    es = torch.empty((num_seqs, num_heads, max_num_partitions), dtype=torch.float32, device=device)
+                    device="cuda", q_len: int = 1):
+    """Allocate (tmp_output, exp_sums, max_logits) once, to be reused across calls.
+
+    Shapes [S, H, NP, D] / [S, H, NP], or [S, Q, H, NP, D] / [S, Q, H, NP] for q_len Q > 1.
+    """
+    lead = (num_seqs, num_heads) if q_len == 1 else (num_seqs, q_len, num_heads)
+    tmp = torch.empty(lead + (max_num_partitions, head_dim), dtype=torch.float32, device=device)
+    es = torch.empty(lead + (max_num_partitions,), dtype=torch.float32, device=device)
     ml = torch.empty_like(es)
     return tmp, es, ml
 
@@ -161,6 +179,30 @@ def pa_decode_v2_phase2(seq_lens, max_seq_len, partition_size, tmp_output, exp_s
                                  _DTYPE[out.dtype], _ptr(tmp_output), _ptr(exp_sums),
                                  _ptr(max_logits), NP, _ptr(out), _ptr(status), _stream(stream))
     _check("pa_decode_v2_phase2", rc)
+    return out
+
+
+def pa_decode_v2_mq(query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
+                    out, tmp_output, exp_sums, max_logits, max_seq_len_hint=0, status=None,
+                    stream=None):
+    """Several new tokens per sequence: query / out [S, Q, H, D], intermediates [S, Q, H, NP, ...]."""
+    lib = load()
+    args = _shape_args_mq(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint,
+                          scale)
+    rc = lib.pa_decode_v2_mq(*args, int(partition_size), _DTYPE[query.dtype], _ptr(out),
+                             _ptr(tmp_output), _ptr(exp_sums), _ptr(max_logits),
+                             tmp_output.shape[-2], _ptr(status), _stream(stream))
+    _check("pa_decode_v2_mq", rc)
+    return out
+
+
+def pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, scale, out,
+                    max_seq_len_hint=0, status=None, stream=None):
+    lib = load()
+    args = _shape_args_mq(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint,
+                          scale)
+    rc = lib.pa_decode_v1_mq(*args, _DTYPE[query.dtype], _ptr(out), _ptr(status), _stream(stream))
+    _check("pa_decode_v1_mq", rc)
     return out
 
 

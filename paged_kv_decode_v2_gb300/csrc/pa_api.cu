@@ -79,7 +79,7 @@ int check_shape(const void *query, const void *key_cache, const void *value_cach
         return PA_ERR_UNSUPPORTED;
     if (block_size != 16 && block_size != 32 && block_size != 64)
         return PA_ERR_UNSUPPORTED;
-    if (num_heads / num_kv_heads > kMaxGroup)
+    if (num_heads / num_kv_heads > kMaxGQA)
         return PA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_kv_heads > 65535)
         return PA_ERR_UNSUPPORTED;
@@ -181,7 +181,7 @@ std::atomic<int> g_occ[kMaxDevices][kKernelSlots][kMaxWarps + 1][kMaxStages + 1]
 // device) and returns that limit, or 0 on error.
 size_t smem_limit(int dev, const AttnLaunch &L)
 {
-    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.p.group, L.v1);
+    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.cta_cols, L.v1);
     const int have = g_smem_limit[dev][slot].load(std::memory_order_acquire);
     if (have > 0)
         return (size_t)have;
@@ -189,7 +189,7 @@ size_t smem_limit(int dev, const AttnLaunch &L)
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 0;
     size_t limit = 0;
-    cudaError_t e = attn_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.p.group, L.v1, optin,
+    cudaError_t e = attn_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.cta_cols, L.v1, optin,
                                                            &limit);
     if (e != cudaSuccess)
         return 0;
@@ -207,11 +207,11 @@ int occupancy(int dev, const AttnLaunch &L, int warps, int stages, size_t limit)
     const size_t smem = attn_smem(L, warps, stages);
     if (smem > limit || warps < 1 || warps > kMaxWarps || stages < 1 || stages > kMaxStages)
         return 0;
-    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.p.group, L.v1);
+    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.cta_cols, L.v1);
     const int c = g_occ[dev][slot][warps][stages].load(std::memory_order_relaxed);
     if (c)
         return c - 1;
-    const int n = attn_ops(L.dtype, L.head_dim)->occupancy(L.block_size, L.p.group, L.v1, warps, smem);
+    const int n = attn_ops(L.dtype, L.head_dim)->occupancy(L.block_size, L.cta_cols, L.v1, warps, smem);
     g_occ[dev][slot][warps][stages].store(n + 1, std::memory_order_relaxed);
     return n;
 }
@@ -230,7 +230,7 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
     const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
     const size_t sb = stage_bytes(L.block_size, L.head_dim);
-    const size_t scratch = warp_scratch_bytes(L.p.group, L.head_dim);
+    const size_t scratch = warp_scratch_bytes(L.cta_cols, L.head_dim);
     auto clampi = [](long long v, int lo, int hi) { return (int)(v < lo ? lo : v > hi ? hi : v); };
     const int w_fit = clampi((long long)(65536 / sb), 1, 4);
     int stages = tune_s > 0 ? tune_s : (L.v1 ? 2 : clampi((long long)(65536 / (w_fit * sb)), 1, 2));
@@ -284,7 +284,8 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
 
 // Builds the attention launch (V2 phase 1 or V1) after validation.
 int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const void *value_cache,
-               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int num_heads,
+               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int q_len,
+               int num_heads,
                int num_kv_heads, int head_dim, int num_blocks, int block_size,
                int max_blocks_per_seq, int cap, float scale, int dtype, bool v1,
                int num_partitions, int partition_size,
@@ -307,6 +308,11 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.num_heads = num_heads;
     p.num_kv_heads = num_kv_heads;
     p.group = num_heads / num_kv_heads;
+    p.q_len = q_len;
+    p.cols = p.group * q_len;
+    // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
+    L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
+    p.col_groups = (p.cols + L.cta_cols - 1) / L.cta_cols;
     p.num_blocks = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.seq_len_cap = cap;
@@ -322,12 +328,23 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     L.block_size = block_size;
     L.dtype = dtype;
     L.v1 = v1;
-    L.grid = dim3(v1 ? 1 : num_partitions, num_kv_heads, num_seqs);
+    // Column groups of one partition are adjacent in x, so they are scheduled
+    // together and their K/V reads meet in L2.
+    L.grid = dim3((unsigned)(v1 ? 1 : num_partitions) * p.col_groups, num_kv_heads, num_seqs);
+    return PA_OK;
+}
+
+int check_q_len(int num_seqs, int q_len)
+{
+    if (q_len < 1)
+        return PA_ERR_INVALID_ARG;
+    if (q_len > kMaxQLen || (long long)num_seqs * q_len > 65535)
+        return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
 int v2_phase1_impl(const void *query, const void *key_cache, const void *value_cache,
-                   const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                   const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int q_len,
                    int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
                    int max_blocks_per_seq, int max_seq_len_hint, float scale, int partition_size,
                    int dtype, float *tmp_output, float *exp_sums, float *max_logits,
@@ -336,6 +353,9 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
     int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                          num_heads, num_kv_heads, head_dim, num_blocks, block_size,
                          max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    rc = check_q_len(num_seqs, q_len);
     if (rc)
         return rc;
     if (partition_size <= 0 || partition_size % block_size != 0)
@@ -353,17 +373,16 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
     if (np == 0)
         return PA_OK;
     AttnLaunch L;
-    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                    num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, cap, scale,
-                    dtype,
-                    false, np, partition_size, tmp_output, exp_sums, max_logits,
+    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                    cap, scale, dtype, false, np, partition_size, tmp_output, exp_sums, max_logits,
                     max_num_partitions, nullptr, status);
     if (rc)
         return rc;
     return prepare_and_launch_attn(L, stream);
 }
 
-int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int head_dim,
+int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_heads, int head_dim,
                    int max_seq_len, int partition_size, int dtype, const float *tmp_output,
                    const float *exp_sums, const float *max_logits, int max_num_partitions,
                    void *out, int32_t *status, cudaStream_t stream)
@@ -377,14 +396,18 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int num_heads, int hea
         return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return PA_ERR_UNSUPPORTED;
-    if (num_seqs > 65535 || num_heads > INT32_MAX / 2)
+    if (num_heads > 65535)
         return PA_ERR_UNSUPPORTED;
+    const int qrc = check_q_len(num_seqs, q_len);
+    if (qrc)
+        return qrc;
     if (!aligned(tmp_output, 16) || !aligned(out, 2))
         return PA_ERR_INVALID_ARG;
     if (pa_v2_num_partitions(max_seq_len, partition_size) > max_num_partitions)
         return PA_ERR_WORKSPACE;
     MergeParams p;
     p.seq_lens = seq_lens;
+    p.q_len = q_len;
     p.num_heads = num_heads;
     p.head_dim = head_dim;
     p.seq_len_cap = max_seq_len;
@@ -445,7 +468,7 @@ PA_API int pa_decode_v2_phase1(const void *query, const void *key_cache, const v
                                float *exp_sums, float *max_logits, int max_num_partitions,
                                int32_t *status, pa_stream_t stream)
 {
-    return v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+    return v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, 1,
                           num_heads, num_kv_heads, head_dim, num_blocks, block_size,
                           max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
                           tmp_output, exp_sums, max_logits, max_num_partitions, status,
@@ -458,9 +481,32 @@ PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_he
                                const float *max_logits, int max_num_partitions, void *out,
                                int32_t *status, pa_stream_t stream)
 {
-    return v2_phase2_impl(seq_lens, num_seqs, num_heads, head_dim, max_seq_len, partition_size,
+    return v2_phase2_impl(seq_lens, num_seqs, 1, num_heads, head_dim, max_seq_len, partition_size,
                           dtype, tmp_output, exp_sums, max_logits, max_num_partitions, out,
                           status, (cudaStream_t)stream);
+}
+
+PA_API int pa_decode_v2_mq(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int q_len, int num_heads, int num_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int max_seq_len_hint, float scale, int partition_size, int dtype,
+                           void *out, float *tmp_output, float *exp_sums, float *max_logits,
+                           int max_num_partitions, int32_t *status, pa_stream_t stream)
+{
+    if (!out || !aligned(out, 2))
+        return PA_ERR_INVALID_ARG;
+    int cap = 0;
+    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
+                            tmp_output, exp_sums, max_logits, max_num_partitions, status,
+                            (cudaStream_t)stream, &cap);
+    if (rc)
+        return rc;
+    return v2_phase2_impl(seq_lens, num_seqs, q_len, num_heads, head_dim, cap, partition_size,
+                          dtype, tmp_output, exp_sums, max_logits, max_num_partitions, out, status,
+                          (cudaStream_t)stream);
 }
 
 PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *value_cache,
@@ -471,19 +517,37 @@ PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *va
                         float *exp_sums, float *max_logits, int max_num_partitions,
                         int32_t *status, pa_stream_t stream)
 {
-    if (!out || !aligned(out, 2))
-        return PA_ERR_INVALID_ARG;
-    int cap = 0;
-    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
-                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
-                            tmp_output, exp_sums, max_logits, max_num_partitions, status,
-                            (cudaStream_t)stream, &cap);
+    return pa_decode_v2_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, 1,
+                           num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                           max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype, out,
+                           tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
+}
+
+PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void *value_cache,
+                           const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                           int q_len, int num_heads, int num_kv_heads, int head_dim,
+                           int num_blocks, int block_size, int max_blocks_per_seq,
+                           int max_seq_len_hint, float scale, int dtype, void *out,
+                           int32_t *status, pa_stream_t stream)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
     if (rc)
         return rc;
-    return v2_phase2_impl(seq_lens, num_seqs, num_heads, head_dim, cap, partition_size, dtype,
-                          tmp_output, exp_sums, max_logits, max_num_partitions, out, status,
-                          (cudaStream_t)stream);
+    rc = check_q_len(num_seqs, q_len);
+    if (rc)
+        return rc;
+    if (!out || !aligned(out, 2))
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    AttnLaunch L;
+    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                    cap, scale, dtype, true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
+    if (rc)
+        return rc;
+    return prepare_and_launch_attn(L, (cudaStream_t)stream);
 }
 
 PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *value_cache,
@@ -492,22 +556,9 @@ PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *va
                         int block_size, int max_blocks_per_seq, int max_seq_len_hint, float scale,
                         int dtype, void *out, int32_t *status, pa_stream_t stream)
 {
-    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
-                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                         max_blocks_per_seq, scale, dtype);
-    if (rc)
-        return rc;
-    if (!out || !aligned(out, 2))
-        return PA_ERR_INVALID_ARG;
-    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
-    AttnLaunch L;
-    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, num_heads,
-                    num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq, cap, scale,
-                    dtype,
-                    true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
-    if (rc)
-        return rc;
-    return prepare_and_launch_attn(L, (cudaStream_t)stream);
+    return pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, 1,
+                           num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                           max_blocks_per_seq, max_seq_len_hint, scale, dtype, out, status, stream);
 }
 
 PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size)

@@ -65,7 +65,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     const int g4 = lane >> 2; // row group of the mma fragments
     const int t4 = lane & 3;  // thread within the group
 
-    const int part = blockIdx.x;
+    // blockIdx.x = partition * col_groups + column group (V1: the column group).
+    const int cgi = V1 ? (int)blockIdx.x : (int)blockIdx.x % p.col_groups;
+    const int part = V1 ? 0 : (int)blockIdx.x / p.col_groups;
     const int kv = blockIdx.y;
     const int b = blockIdx.z;
 
@@ -83,6 +85,14 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // ---- loads that do not depend on the sequence length, issued together:
     // the length, the first two chunks of block ids and the Q fragments.
     const int head0 = kv * p.group;
+    // Columns of this CTA: query rows (new token i, head head0 + g) for the
+    // global column c = col0 + n = i * group + g, n < ncols.
+    const int col0 = cgi * kHeads;
+    const int ncols = min(kHeads, p.cols - col0);
+    auto col_row = [&](int n) -> size_t { // row of [S * q_len * H] for local column n
+        const int c = col0 + n;
+        return ((size_t)b * p.q_len + c / p.group) * p.num_heads + head0 + c % p.group;
+    };
     const int blk0 = V1 ? 0 : part * p.part_blocks;
     const int range_max = V1 ? p.max_blocks : min(p.part_blocks, p.max_blocks - blk0);
     const int cnt_max = warp < range_max ? (range_max - warp + nwarps - 1) / nwarps : 0;
@@ -101,9 +111,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
         const uint32_t *q32 = static_cast<const uint32_t *>(p.query);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            const int g = j * 8 + g4;
-            const bool has = g < p.group;
-            const size_t rowbase = ((size_t)b * p.num_heads + head0 + (has ? g : 0)) * (D / 2);
+            const int n = j * 8 + g4;
+            const bool has = n < ncols;
+            const size_t rowbase = col_row(has ? n : 0) * (D / 2);
 #pragma unroll
             for (int ks = 0; ks < kKS; ++ks) {
                 qf[j][ks][0] = has ? __ldg(q32 + rowbase + ks * 8 + t4) : 0u;
@@ -127,10 +137,22 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
 
     if (V1 && nblk == 0) { // empty sequence: zero output
         T *out = static_cast<T *>(p.out);
-        for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x)
-            out[((size_t)b * p.num_heads + head0) * D + idx] = E::from_float(0.f);
+        for (int idx = threadIdx.x; idx < ncols * D; idx += blockDim.x)
+            out[col_row(idx / D) * D + idx % D] = E::from_float(0.f);
         return;
     }
+
+    // Causal limit of this lane's columns 8j + 2t4 (+1), in tokens from the
+    // start of the CTA's range: new token i sees positions <= L - q_len + i.
+    // Padding columns (past ncols) keep the whole range and are never stored.
+    int lim[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int n = j * 8 + 2 * t4 + k;
+            lim[j][k] = (n < ncols ? L - p.q_len + (col0 + n) / p.group : L - 1) - tok0;
+        }
 
     const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
     const uint32_t ring = smem0 + (uint32_t)warp * (uint32_t)p.stages * kStageBytes;
@@ -265,17 +287,16 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
             }
 
             // ---- scale, mask, streaming softmax update
-            const int r0 = tile * 16 + g4; // token rows of c0/c1 and (r0 + 8) of c2/c3
-            const bool ok0 = r0 < valid;
-            const bool ok1 = r0 + 8 < valid;
+            // token rows of c0/c1 and (r0 + 8) of c2/c3, from the start of the range
+            const int r0 = jblk * BS + tile * 16 + g4;
             uint32_t pb[NT][2][2]; // [n-tile][hi/lo][b0/b1]
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 float sv[4];
-                sv[0] = ok0 ? sacc[j][0] * scale : -INFINITY;
-                sv[1] = ok0 ? sacc[j][1] * scale : -INFINITY;
-                sv[2] = ok1 ? sacc[j][2] * scale : -INFINITY;
-                sv[3] = ok1 ? sacc[j][3] * scale : -INFINITY;
+                sv[0] = r0 <= lim[j][0] ? sacc[j][0] * scale : -INFINITY;
+                sv[1] = r0 <= lim[j][1] ? sacc[j][1] * scale : -INFINITY;
+                sv[2] = r0 + 8 <= lim[j][0] ? sacc[j][2] * scale : -INFINITY;
+                sv[3] = r0 + 8 <= lim[j][1] ? sacc[j][3] * scale : -INFINITY;
                 float mx0 = fmaxf(sv[0], sv[2]);
                 float mx1 = fmaxf(sv[1], sv[3]);
 #pragma unroll
@@ -285,11 +306,13 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
                 }
                 const float mn0 = fmaxf(m_run[j][0], mx0);
                 const float mn1 = fmaxf(m_run[j][1], mx1);
-                const float a0 = fast_exp2((m_run[j][0] - mn0) * kLog2e);
-                const float a1 = fast_exp2((m_run[j][1] - mn1) * kLog2e);
+                // A column with no visible token yet (max still -inf) keeps l = o = 0.
+                const bool live0 = mn0 != -INFINITY, live1 = mn1 != -INFINITY;
+                const float a0 = live0 ? fast_exp2((m_run[j][0] - mn0) * kLog2e) : 1.f;
+                const float a1 = live1 ? fast_exp2((m_run[j][1] - mn1) * kLog2e) : 1.f;
                 m_run[j][0] = mn0;
                 m_run[j][1] = mn1;
-                const float mb0 = mn0 * kLog2e, mb1 = mn1 * kLog2e;
+                const float mb0 = live0 ? mn0 * kLog2e : 0.f, mb1 = live1 ? mn1 * kLog2e : 0.f;
                 float pv[4];
                 pv[0] = fast_exp2(fmaf(sv[0], kLog2e, -mb0));
                 pv[1] = fast_exp2(fmaf(sv[1], kLog2e, -mb1));
@@ -389,7 +412,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     // ---- merge the warps: M = max m_w, f_w = exp(m_w - M), l = sum f_w l_w, o = sum f_w o_w / l
     const uint32_t warp_stride = (uint32_t)stages * kStageBytes / 4; // floats between warp scratches
     const float *scr0 = reinterpret_cast<const float *>(dyn_smem + (smem0 - smem_addr(dyn_smem)));
-    if (threadIdx.x < p.group) {
+    if (threadIdx.x < ncols) {
         const int h = threadIdx.x;
         float M = -INFINITY;
         for (int w = 0; w < nwarps; ++w)
@@ -406,15 +429,17 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < ncols * D; idx += blockDim.x) {
         const int h = idx / D;
         const int d = idx % D;
         float acc = 0.f;
         for (int w = 0; w < nwarps; ++w)
             acc = fmaf(s_factor[w][h], scr0[w * warp_stride + 2 * kHeads + h * kScr + d], acc);
         const float lsum = s_stat[1][h];
-        const float val = acc / lsum;
-        const size_t bh = (size_t)b * p.num_heads + head0 + h;
+        // lsum == 0: no token of this range is visible to the column (only with
+        // several new tokens): an empty partition, or a zero output in V1.
+        const float val = lsum > 0.f ? acc / lsum : 0.f;
+        const size_t bh = col_row(h);
         if (V1) {
             static_cast<T *>(p.out)[bh * D + d] = E::from_float(val);
         } else {
@@ -428,11 +453,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1)
     }
 }
 
-// Kernel dispatch on block size, n-tiles (G <= 8 or <= 16) and V1/V2, for one head_dim.
+// Kernel dispatch on block size, n-tiles (<= 8 or <= 16 columns) and V1/V2, for one head_dim.
 template <typename T, int D>
-static const void *attn_kernel_ptr(int block_size, int group, bool v1)
+static const void *attn_kernel_ptr(int block_size, int cols, bool v1)
 {
-    const bool nt2 = group > 8;
+    const bool nt2 = cols > 8;
 #define PA_PICK(BS)                                                                               \
     if (block_size == BS) {                                                                       \
         if (nt2)                                                                                  \
@@ -451,9 +476,9 @@ static const void *attn_kernel_ptr(int block_size, int group, bool v1)
 // Opts the kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory; returns that limit in *limit.
 template <typename T, int D>
-static cudaError_t attn_prepare(int block_size, int group, bool v1, int optin_bytes, size_t *limit)
+static cudaError_t attn_prepare(int block_size, int cols, bool v1, int optin_bytes, size_t *limit)
 {
-    const void *fn = attn_kernel_ptr<T, D>(block_size, group, v1);
+    const void *fn = attn_kernel_ptr<T, D>(block_size, cols, v1);
     if (!fn)
         return cudaErrorInvalidValue;
     cudaFuncAttributes fa;
@@ -468,9 +493,9 @@ static cudaError_t attn_prepare(int block_size, int group, bool v1, int optin_by
 
 // Resident CTAs per SM for a launch shape (0 on error).
 template <typename T, int D>
-static int attn_occupancy(int block_size, int group, bool v1, int warps, size_t smem_bytes)
+static int attn_occupancy(int block_size, int cols, bool v1, int warps, size_t smem_bytes)
 {
-    const void *fn = attn_kernel_ptr<T, D>(block_size, group, v1);
+    const void *fn = attn_kernel_ptr<T, D>(block_size, cols, v1);
     int n = 0;
     if (!fn || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, warps * 32, smem_bytes) !=
                    cudaSuccess)
@@ -481,7 +506,7 @@ static int attn_occupancy(int block_size, int group, bool v1, int warps, size_t 
 template <typename T, int D>
 static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
 {
-    const void *fn = attn_kernel_ptr<T, D>(L.block_size, L.p.group, L.v1);
+    const void *fn = attn_kernel_ptr<T, D>(L.block_size, L.cta_cols, L.v1);
     if (!fn)
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),

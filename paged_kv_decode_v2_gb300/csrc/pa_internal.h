@@ -10,19 +10,24 @@
 
 namespace pa {
 
-constexpr int kMaxGroup = 16;        // query heads per KV head
+constexpr int kMaxGroup = 16;        // query rows (columns) one attention CTA serves
+constexpr int kMaxQLen = 64;         // new tokens per sequence
+constexpr int kMaxGQA = 64;          // query heads per KV head
 constexpr int kMaxWarps = 8;         // warps per attention CTA
 constexpr int kMaxStages = 8;        // TMA ring stages per warp
 constexpr int kMergeThreads = 128;   // phase-2 CTA size
 
 // Arguments of the attention kernel (phase 1 of V2, or V1).
 struct AttnParams {
-    const void *query;           // [S, H, D]
+    const void *query;           // [S, q_len, H, D]
     const int32_t *block_tables; // [S, max_blocks]
     const int32_t *seq_lens;     // [S]
     int num_heads;
     int num_kv_heads;
     int group;                   // G = H / KV
+    int q_len;                   // new tokens per sequence (query rows per (seq, head))
+    int cols;                    // G * q_len query rows per KV head
+    int col_groups;              // CTAs that split those rows (16 rows each when > 1)
     int num_blocks;
     int max_blocks;
     int seq_len_cap;             // lengths are clamped to [0, cap]
@@ -30,10 +35,10 @@ struct AttnParams {
     int part_blocks;             // V2: blocks per partition
     int stages;                  // TMA ring stages per warp
     int max_num_partitions;      // V2: partition capacity of the intermediates
-    float *tmp_output;           // V2: [S, H, NPcap, D]
-    float *exp_sums;             // V2: [S, H, NPcap]
-    float *max_logits;           // V2: [S, H, NPcap]
-    void *out;                   // V1: [S, H, D]
+    float *tmp_output;           // V2: [S, q_len, H, NPcap, D]
+    float *exp_sums;             // V2: [S, q_len, H, NPcap]
+    float *max_logits;           // V2: [S, q_len, H, NPcap]
+    void *out;                   // V1: [S, q_len, H, D]
     int32_t *status;
 };
 
@@ -45,6 +50,7 @@ struct AttnLaunch {
     int block_size;              // 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
+    int cta_cols;                // query rows one CTA serves (<= 16): picks the n-tile count
     dim3 grid;
     int warps;
     size_t smem_bytes;
@@ -52,6 +58,7 @@ struct AttnLaunch {
 
 struct MergeParams {
     const int32_t *seq_lens;
+    int q_len;                   // rows of the grid's y dimension are (sequence, new token)
     int num_heads;
     int head_dim;
     int seq_len_cap;
@@ -72,16 +79,16 @@ inline size_t stage_bytes(int block_size, int head_dim)
 }
 
 // Scratch one warp needs to hand its partial {m, l, o} to the CTA merge.
-inline size_t warp_scratch_bytes(int group, int head_dim)
+inline size_t warp_scratch_bytes(int cta_cols, int head_dim)
 {
-    int heads = group <= 8 ? 8 : 16;
+    int heads = cta_cols <= 8 ? 8 : 16;
     return static_cast<size_t>(heads) * (2 + head_dim + 4) * 4;
 }
 
 // Entry points of the attention kernels for one (storage type, head_dim).
 struct AttnOps {
-    cudaError_t (*prepare)(int block_size, int group, bool v1, int optin_bytes, size_t *limit);
-    int (*occupancy)(int block_size, int group, bool v1, int warps, size_t smem_bytes);
+    cudaError_t (*prepare)(int block_size, int cta_cols, bool v1, int optin_bytes, size_t *limit);
+    int (*occupancy)(int block_size, int cta_cols, bool v1, int warps, size_t smem_bytes);
     cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
 };
 const AttnOps *attn_ops_f16_d64();

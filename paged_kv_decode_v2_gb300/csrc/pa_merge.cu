@@ -27,7 +27,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     __shared__ float4 s_acc[kSlots][kGroup];
 
     const int h = blockIdx.x;
-    const int b = blockIdx.y;
+    const int row = blockIdx.y;       // (sequence, new token) = b * q_len + i
+    const int b = row / p.q_len;
     const int D = p.head_dim;
     const int d0 = blockIdx.z * DD;
     const int slot = threadIdx.x / kGroup; // partitions slot, slot + kSlots, ...
@@ -40,7 +41,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     int L = __ldg(&p.seq_lens[b]);
     L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
     const int np = (L + p.partition_size - 1) / p.partition_size;
-    const size_t bh = (size_t)b * p.num_heads + h;
+    const size_t bh = (size_t)row * p.num_heads + h;
     T *out = static_cast<T *>(p.out) + bh * D + d0;
     if (np == 0) {
         if (threadIdx.x < DD)
@@ -65,6 +66,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         const float mp = __ldg(ml + i);
         const float lp = __ldg(es + i);
         const float4 v = __ldg(tmp + (size_t)i * row4 + c);
+        if (lp == 0.f) // a partition none of whose tokens this query sees
+            continue;
         const float mn = fmaxf(m, mp);
         const float a = fast_exp2((m - mn) * kLog2e); // 0 while m is -inf
         const float w = fast_exp2((mp - mn) * kLog2e) * lp;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
             const float *a = reinterpret_cast<const float *>(&s_acc[s][d >> 2]);
             o = fmaf(f, a[d & 3], o);
         }
-        out[d] = E::from_float(o / total);
+        out[d] = E::from_float(total > 0.f ? o / total : 0.f); // 0: the query sees no token
     }
 }
 
@@ -117,12 +120,12 @@ cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_
     // A CTA owns at most 128 dims of head_dim; split further (down to 16
     // dims) while the grid has fewer than about two CTAs per SM -- a finer
     // split only adds CTAs of very little work.
-    const long long pairs = (long long)p.num_heads * num_seqs;
+    const long long pairs = (long long)p.num_heads * num_seqs * p.q_len;
     int dd = p.head_dim < 128 ? p.head_dim : 128;
     while (dd > 16 && pairs * (p.head_dim / dd) < 2LL * num_sms)
         dd /= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_heads, num_seqs, p.head_dim / dd);
+    cfg.gridDim = dim3(p.num_heads, num_seqs * p.q_len, p.head_dim / dd);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -122,10 +122,17 @@ def check_partitions(inp: wl.Inputs, P: int, tmp, es, ml, pairs=None, prob=None)
         dt = np.abs(tmp_c[b, h, :n] - o[i, :n])
         assert np.isfinite(tmp_c[b, h, :n]).all()
         assert dt.max() <= TMP_ABS, f"tmp_output ({b},{h}) err {dt.max():.3e}"
-        dm = np.abs(ml_c[b, h, :n] - m[i, :n])
-        assert (dm <= MAXLOGIT_REL * np.maximum(1.0, np.abs(m[i, :n]))).all(), \
+        # Empty partitions (a query that sees none of their tokens): l = 0, m = -inf.
+        empty = l[i, :n] == 0.0
+        assert (es_c[b, h, :n][empty] == 0.0).all(), f"exp_sums ({b},{h}) of an empty partition"
+        assert (ml_c[b, h, :n][empty] == -np.inf).all(), f"max_logits ({b},{h}) of an empty partition"
+        full = ~empty
+        if not full.any():
+            continue
+        dm = np.abs(ml_c[b, h, :n][full] - m[i, :n][full])
+        assert (dm <= MAXLOGIT_REL * np.maximum(1.0, np.abs(m[i, :n][full]))).all(), \
             f"max_logits ({b},{h}) err {dm.max():.3e}"
-        de = np.abs(es_c[b, h, :n] - l[i, :n]) / l[i, :n]
+        de = np.abs(es_c[b, h, :n][full] - l[i, :n][full]) / l[i, :n][full]
         assert (de <= EXPSUM_REL).all(), f"exp_sums ({b},{h}) rel err {de.max():.3e}"
         worst = [max(worst[0], dt.max()), max(worst[1], dm.max()), max(worst[2], de.max())]
     return worst

@@ -1,0 +1,118 @@
+"""GPU parity for several new tokens per sequence (q_len > 1, causal prefix).
+
+New token i of a sequence with L tokens (the q_len new ones included) sees
+keys t <= L - q_len + i.  The CUDA path (pa_decode_v2_mq / pa_decode_v1_mq
+through the C ABI) is compared element by element with the fp64 oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from parity_util import check_out, check_partitions, oracle_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    cuda_lib.pa_set_launch_config(0, 0)
+
+
+def run_mq(inp, P, entry="v2", hint=0, status=None):
+    import paged_kv_decode_v2_gb300 as pa
+    w = inp.workload
+    S, Q, H, D = inp.query.shape
+    cap = inp.block_tables.shape[1] * w.block_size
+    if hint > 0:
+        cap = min(cap, hint)
+    npmax = max(1, pa.num_partitions(cap, P))
+    tmp, es, ml = pa.alloc_workspace(S, H, D, npmax, q_len=Q)
+    for t in (tmp, es, ml):
+        t.fill_(float("nan"))
+    out = torch.full_like(inp.query, float("nan"))
+    args = (inp.query, inp.key_cache, inp.value_cache, inp.block_tables, inp.seq_lens, w.scale)
+    if entry == "v2":
+        pa.pa_decode_v2_mq(*args, P, out, tmp, es, ml, max_seq_len_hint=hint, status=status)
+    else:
+        pa.pa_decode_v1_mq(*args, out, max_seq_len_hint=hint, status=status)
+    torch.cuda.synchronize()
+    return out, tmp, es, ml
+
+
+def check_mq(inp, P, entries=("v2", "v1")):
+    prob = oracle_problem(inp)
+    ref = oracle.decode(prob)  # [S, Q, H, D]
+    S, Q, H, D = inp.query.shape
+    for e in entries:
+        out, tmp, es, ml = run_mq(inp, P, entry=e)
+        check_out(out, ref, inp.workload.dtype, what=f"{inp.workload.name}/{e}")
+        if e == "v2":
+            pairs = [(r, h) for r in range(S * Q) for h in range(H)]
+            check_partitions(inp, P, tmp.view(S * Q, H, *tmp.shape[3:]), es.view(S * Q, H, -1),
+                             ml.view(S * Q, H, -1), pairs=pairs, prob=prob)
+    return ref
+
+
+def mq(name, q_len, G, lens, bs=16, P=64, dtype=wl.BF16, D=128, KV=2, seed=0):
+    return wl.Workload(name, len(lens), G * KV, KV, D, bs, P, dtype, "list", seq_lens=tuple(lens),
+                       q_len=q_len, seed=seed)
+
+
+@pytest.mark.parametrize("q_len", [2, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_mq_fuzz(q_len, G, dtype):
+    P = 64
+    lens = (1, q_len - 1 or 1, q_len, P - 1, P, P + 1, P + q_len, 3 * P + 5, 200)
+    w = mq("mq_fuzz", q_len, G, lens, P=P, dtype=dtype, seed=4000 + 13 * q_len + G + dtype)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("q_len,G", [(4, 8), (8, 4), (3, 16), (64, 1), (16, 8)])
+def test_mq_rows_split_over_ctas(q_len, G):
+    """More than 16 query rows per KV head: rows split over side-by-side CTAs."""
+    lens = (q_len, 2 * q_len + 3, 700)
+    w = mq("mq_split", q_len, G, lens, P=256, seed=5000 + q_len + G)
+    check_mq(wl.make_inputs(w, device="cuda"), 256)
+
+
+@pytest.mark.parametrize("D,bs", [(64, 32), (256, 16), (128, 64)])
+def test_mq_other_shapes(D, bs):
+    w = mq("mq_shapes", 4, 4, (5, 130, 333), bs=bs, P=128, D=D, seed=6000 + D + bs)
+    check_mq(wl.make_inputs(w, device="cuda"), 128)
+
+
+def test_mq_single_token_matches_the_single_query_entry():
+    import paged_kv_decode_v2_gb300 as pa
+    inp = wl.make_inputs(wl.TINY, device="cuda")
+    S, H, D = inp.query.shape
+    tmp, es, ml = pa.alloc_workspace(S, H, D, 2)
+    a = torch.empty_like(inp.query)
+    pa.pa_decode_v2(inp.query, inp.key_cache, inp.value_cache, inp.block_tables, inp.seq_lens,
+                    wl.TINY.scale, 512, a, tmp, es, ml)
+    b = torch.empty_like(inp.query)[:, None]
+    tmp2, es2, ml2 = pa.alloc_workspace(S, H, D, 2, q_len=1)
+    pa.pa_decode_v2_mq(inp.query[:, None].contiguous(), inp.key_cache, inp.value_cache,
+                       inp.block_tables, inp.seq_lens, wl.TINY.scale, 512, b, tmp2, es2, ml2)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b[:, 0])
+
+
+def test_mq_speculative_batch_full_size():
+    """Batch decode (32 seqs up to 8192 tokens, 32/8 heads) checking 4 speculated tokens each."""
+    w = wl.BATCH.with_(name="batch_spec4", q_len=4)
+    inp = wl.make_inputs(w, device="cuda")
+    check_mq(inp, w.partition_size)
+
+
+def test_mq_rejects_bad_q_len(cuda_lib):
+    lib = cuda_lib.load()
+    FAKE = 0x10000
+    args = [FAKE] * 5 + [1, 0, 8, 2, 128, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_v1_mq(*args, 0, FAKE, None, None) == cuda_lib.PA_ERR_INVALID_ARG
+    args = [FAKE] * 5 + [1, 65, 8, 2, 128, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_v1_mq(*args, 0, FAKE, None, None) == cuda_lib.PA_ERR_UNSUPPORTED
