@@ -186,19 +186,29 @@ class Decoder:
             v = torch.randn(base.value_cache.shape, generator=g, device=device).to(base.value_cache.dtype)
             self.caches.append((k, v))
         self.inp = base
-        S, H, D = base.query.shape
+        S, H, D = base.query.shape[0], w.num_heads, w.head_dim
         self.cap = base.block_tables.shape[1] * w.block_size
         self.max_seq_len = base.max_seq_len
         self.np = pa.num_partitions(self.max_seq_len, w.partition_size)
-        self.tmp, self.es, self.ml = pa.alloc_workspace(S, H, D, max(1, self.np), device=device)
+        self.tmp, self.es, self.ml = pa.alloc_workspace(S, H, D, max(1, self.np), device=device,
+                                                        q_len=w.q_len)
         self.out = torch.empty_like(base.query)
-        self.variant = pa.pa_decode_choose(S, w.num_kv_heads, self.max_seq_len, w.partition_size)
+        if w.q_len > 1:
+            self.variant = 2  # several new tokens: the two-pass multi-query entry point
+        else:
+            self.variant = pa.pa_decode_choose(S, w.num_kv_heads, self.max_seq_len,
+                                               w.partition_size)
         self.launches_per_step = 2 if self.variant == 2 else 1
 
     def call(self, i: int):
         """One decode call on copy i % R through the public dispatch entry point."""
         pa, w, inp = self.pa, self.w, self.inp
         kc, vc = self.caches[i % self.copies]
+        if w.q_len > 1:
+            pa.pa_decode_v2_mq(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
+                               w.partition_size, self.out, self.tmp, self.es, self.ml,
+                               max_seq_len_hint=self.max_seq_len)
+            return
         pa.pa_decode(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, w.partition_size,
                      self.out, self.tmp, self.es, self.ml, max_seq_len_hint=self.max_seq_len)
 
@@ -207,7 +217,10 @@ class Decoder:
         pa, w, inp = self.pa, self.w, self.inp
         kc, vc = self.caches[i % self.copies]
         ev[0].record()
-        if self.variant == 2:
+        if w.q_len > 1:  # no separate phase entry points: the whole call is timed
+            self.call(i)
+            ev[1].record()
+        elif self.variant == 2:
             pa.pa_decode_v2_phase1(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
                                    w.partition_size, self.tmp, self.es, self.ml,
                                    max_seq_len_hint=self.max_seq_len)
@@ -345,8 +358,10 @@ def time_gpu(args, w: wl.Workload):
                      "frac": round(k1_gbs / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec.kv_bytes,
                      "kernel_us": round(k1_ms * 1e3, 3),
-                     "timing": "kernel 1 alone, CUDA events around it on its stream, "
-                               "averaged over K split calls right after the timed region",
+                     "timing": ("kernel 1 alone, CUDA events around it on its stream, "
+                                "averaged over K split calls right after the timed region")
+                               if w.q_len == 1 else
+                               "whole call (both kernels), CUDA events, K calls after the timed region",
                      "merge_us": round(k2_ms * 1e3, 3) if dec.variant == 2 else None},
         "clocks": clocks,
     }

@@ -28,7 +28,8 @@
  * walks every block with a running {m, l, o}; "vllm/_custom_ops.py" commit
  * 900ae0b, "V1: 1 CTA iterates ... partitions sequentially").  pa_decode
  * chooses between them ("paged_attn.py" commit 490ff98, change 1: restore
- * the V1/V2 adaptive dispatch), with a rule re-derived for this GPU.
+ * the V1/V2 adaptive dispatch), with a rule re-measured on this GPU: V1
+ * when the longest sequence fits one partition, else V2.
  *
  * Layouts (all row-major, contiguous, device memory)
  * --------------------------------------------------

@@ -40,8 +40,19 @@
 
 namespace pa {
 
+// Phase-1 CTAs that serve 16 query rows (NT = 2) of up to 128 dims run at
+// most 4 warps, so that three CTAs fit an SM (<= 170 registers, no spills);
+// every other kernel runs up to 8 warps.
+template <int D, int NT, bool V1>
+struct AttnBounds {
+    static constexpr bool kNarrow = NT == 2 && !V1 && D <= 128;
+    static constexpr int kThreads = kNarrow ? 128 : kMaxWarps * 32;
+    static constexpr int kMinBlocks = kNarrow ? 3 : 1;
+};
+
 template <typename T, int D, int BS, int NT, bool V1>
-__global__ void __launch_bounds__(kMaxWarps * 32, 1)
+__global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
+                                  AttnBounds<D, NT, V1>::kMinBlocks)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
 {

@@ -79,7 +79,10 @@ RAGGED = Workload("ragged_serving", 64, 64, 8, 128, 32, 512, BF16, "lognormal", 
 STRESS = Workload("stress", 8, 64, 8, 128, 16, 1024, F16, "fixed", seq_len=131072,
                   pool_blocks=70000, seed=20261206)
 
-ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS)}
+# Batch decode checking 4 speculated tokens per sequence (several new tokens per call).
+BATCH_SPEC4 = BATCH.with_(name="batch_decode_spec4", q_len=4)
+
+ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS, BATCH_SPEC4)}
 
 
 def draw_seq_lens(w: Workload) -> list:
