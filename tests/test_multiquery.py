@@ -116,3 +116,26 @@ def test_mq_rejects_bad_q_len(cuda_lib):
     assert lib.pa_decode_v1_mq(*args, 0, FAKE, None, None) == cuda_lib.PA_ERR_INVALID_ARG
     args = [FAKE] * 5 + [1, 65, 8, 2, 128, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_v1_mq(*args, 0, FAKE, None, None) == cuda_lib.PA_ERR_UNSUPPORTED
+
+
+def test_mq_unreferenced_slots_and_relabelling():
+    """Poison never reaches the output; relabelling physical blocks changes nothing (bitwise)."""
+    w = mq("mq_poison", 4, 4, (3, 37, 200, 64), bs=16, P=64, seed=77)
+    inp = wl.make_inputs(w, device="cuda", max_blocks=20)
+    clean = [run_mq(inp, 64, entry=e)[0] for e in ("v2", "v1")]
+    wl.poison_unreferenced(inp, float("nan"))
+    for a, e in zip(clean, ("v2", "v1")):
+        assert torch.equal(a, run_mq(inp, 64, entry=e)[0])
+    r = wl.relabel_blocks(inp, seed=9)
+    for a, e in zip(clean, ("v2", "v1")):
+        assert torch.equal(a, run_mq(r, 64, entry=e)[0])
+
+
+def test_mq_bad_block_id_sets_status():
+    w = mq("mq_status", 2, 4, (100, 300), P=64, seed=78)
+    inp = wl.make_inputs(w, device="cuda")
+    inp.block_tables[1, 3] = inp.key_cache.shape[0] + 1
+    for e in ("v2", "v1"):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        run_mq(inp, 64, entry=e, status=st)
+        assert int(st.item()) & 1

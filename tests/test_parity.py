@@ -191,7 +191,16 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
 
 def test_batch_decode_full_size_every_element():
     inp = wl.make_inputs(wl.BATCH, device="cuda")
-    full_check(inp, wl.BATCH.partition_size, entries=("v2", "dispatch"))
+    full_check(inp, wl.BATCH.partition_size, entries=("v2", "v1", "dispatch"))
+
+
+def test_dispatch_rule(cuda_lib):
+    """V1 when the longest sequence fits one partition, else V2."""
+    assert cuda_lib.pa_decode_choose(32, 8, 512, 512) == 1
+    assert cuda_lib.pa_decode_choose(4096, 8, 300, 512) == 1
+    assert cuda_lib.pa_decode_choose(1, 4, 513, 512) == 2
+    assert cuda_lib.pa_decode_choose(512, 8, 1024, 512) == 2
+    assert cuda_lib.pa_decode_choose(1, 4, 100000, 1024) == 2
 
 
 @pytest.mark.parametrize("P", [512, 1024])
