@@ -49,7 +49,8 @@
  *   A sequence with seq_len 0 gets a zero output row.
  *
  * Supported shapes: head_dim 64, 128 or 256; block_size 16, 32 or 64;
- * partition_size a positive multiple of block_size; G = num_heads /
+ * partition_size any positive value (a partition may begin or end inside a
+ * block; a block that straddles two partitions is read by both); G = num_heads /
  * num_kv_heads an integer in [1, 64]; q_len in [1, 64] with num_seqs *
  * q_len <= 65535 (the _mq entry points).  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned

@@ -321,7 +321,7 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.max_blocks = max_blocks_per_seq;
     p.seq_len_cap = cap;
     p.scale = scale;
-    p.part_blocks = v1 ? 0 : partition_size / block_size;
+    p.partition_size = v1 ? 0 : partition_size;
     p.max_num_partitions = max_num_partitions;
     p.tmp_output = tmp_output;
     p.exp_sums = exp_sums;
@@ -362,7 +362,7 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
     rc = check_q_len(num_seqs, q_len);
     if (rc)
         return rc;
-    if (partition_size <= 0 || partition_size % block_size != 0)
+    if (partition_size <= 0)
         return PA_ERR_INVALID_ARG;
     if (!tmp_output || !exp_sums || !max_logits || max_num_partitions <= 0)
         return PA_ERR_INVALID_ARG;
@@ -589,7 +589,7 @@ PA_API int pa_decode(const void *query, const void *key_cache, const void *value
                          max_blocks_per_seq, scale, dtype);
     if (rc)
         return rc;
-    if (partition_size <= 0 || partition_size % block_size != 0)
+    if (partition_size <= 0)
         return PA_ERR_INVALID_ARG;
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     const int which = pa_decode_choose(num_seqs, num_kv_heads, cap, partition_size);

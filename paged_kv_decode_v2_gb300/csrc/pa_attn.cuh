@@ -104,8 +104,14 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         const int c = col0 + n;
         return ((size_t)b * p.q_len + c / p.group) * p.num_heads + head0 + c % p.group;
     };
-    const int blk0 = V1 ? 0 : part * p.part_blocks;
-    const int range_max = V1 ? p.max_blocks : min(p.part_blocks, p.max_blocks - blk0);
+    // V2: partition `part` holds tokens [tokA, tokA + partition_size), which
+    // may begin and end inside a block; blocks from blk0 cover it.
+    const int tokA = V1 ? 0 : part * p.partition_size;
+    const int blk0 = tokA / BS;
+    const int range_max =
+        V1 ? p.max_blocks
+           : (int)min(((long long)tokA + p.partition_size + BS - 1) / BS, (long long)p.max_blocks) -
+                 blk0;
     const int cnt_max = warp < range_max ? (range_max - warp + nwarps - 1) / nwarps : 0;
     const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
     const int Lraw = __ldg(&p.seq_lens[b]);
@@ -140,10 +146,13 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             set_status(p.status, PA_STATUS_BAD_SEQ_LEN);
         L = L < 0 ? 0 : p.seq_len_cap;
     }
-    const int tok0 = blk0 * BS;
-    if (!V1 && tok0 >= L)
+    if (!V1 && tokA >= L)
         return; // partition past the end of this sequence: nothing to write
-    const int ntok = V1 ? L : min(p.part_blocks * BS, L - tok0);
+    // Token positions below are counted from tok0, the first token of block blk0;
+    // the range is [lo, ntok) of them.
+    const int tok0 = blk0 * BS;
+    const int lo = tokA - tok0;
+    const int ntok = V1 ? L : (int)(min((long long)tokA + p.partition_size, (long long)L) - tok0);
     const int nblk = (ntok + BS - 1) / BS;
 
     if (V1 && nblk == 0) { // empty sequence: zero output
@@ -153,16 +162,18 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         return;
     }
 
-    // Causal limit of this lane's columns 8j + 2t4 (+1), in tokens from the
-    // start of the CTA's range: new token i sees positions <= L - q_len + i.
-    // Padding columns (past ncols) keep the whole range and are never stored.
-    int lim[NT][2];
+    // Visible tokens of this lane's columns 8j + 2t4 (+1): position t - tok0 = lo + r
+    // with r < vis: new token i sees positions <= L - q_len + i, and none
+    // before tokA.  Padding columns (past ncols) keep the whole range and are
+    // never stored.
+    unsigned vis[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int n = j * 8 + 2 * t4 + k;
-            lim[j][k] = (n < ncols ? L - p.q_len + (col0 + n) / p.group : L - 1) - tok0;
+            const int last = (n < ncols ? L - p.q_len + (col0 + n) / p.group : L - 1) - tok0;
+            vis[j][k] = (unsigned)max(last - lo + 1, 0);
         }
 
     const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
@@ -298,16 +309,17 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             }
 
             // ---- scale, mask, streaming softmax update
-            // token rows of c0/c1 and (r0 + 8) of c2/c3, from the start of the range
-            const int r0 = jblk * BS + tile * 16 + g4;
+            // token rows of c0/c1 and (r0 + 8) of c2/c3, from tok0 + lo (an
+            // unsigned compare with vis also masks the rows before lo)
+            const unsigned r0 = (unsigned)(jblk * BS + tile * 16 + g4 - lo);
             uint32_t pb[NT][2][2]; // [n-tile][hi/lo][b0/b1]
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 float sv[4];
-                sv[0] = r0 <= lim[j][0] ? sacc[j][0] * scale : -INFINITY;
-                sv[1] = r0 <= lim[j][1] ? sacc[j][1] * scale : -INFINITY;
-                sv[2] = r0 + 8 <= lim[j][0] ? sacc[j][2] * scale : -INFINITY;
-                sv[3] = r0 + 8 <= lim[j][1] ? sacc[j][3] * scale : -INFINITY;
+                sv[0] = r0 < vis[j][0] ? sacc[j][0] * scale : -INFINITY;
+                sv[1] = r0 < vis[j][1] ? sacc[j][1] * scale : -INFINITY;
+                sv[2] = r0 + 8u < vis[j][0] ? sacc[j][2] * scale : -INFINITY;
+                sv[3] = r0 + 8u < vis[j][1] ? sacc[j][3] * scale : -INFINITY;
                 float mx0 = fmaxf(sv[0], sv[2]);
                 float mx1 = fmaxf(sv[1], sv[3]);
 #pragma unroll

@@ -32,7 +32,7 @@ struct AttnParams {
     int max_blocks;
     int seq_len_cap;             // lengths are clamped to [0, cap]
     float scale;
-    int part_blocks;             // V2: blocks per partition
+    int partition_size;          // V2: tokens per partition (any positive value)
     int stages;                  // TMA ring stages per warp
     int max_num_partitions;      // V2: partition capacity of the intermediates
     float *tmp_output;           // V2: [S, q_len, H, NPcap, D]

@@ -86,6 +86,13 @@ def test_mq_other_shapes(D, bs):
     check_mq(wl.make_inputs(w, device="cuda"), 128)
 
 
+@pytest.mark.parametrize("q_len,G,bs,P", [(3, 4, 16, 300), (4, 8, 32, 40), (8, 2, 64, 100)])
+def test_mq_partition_not_a_multiple_of_block_size(q_len, G, bs, P):
+    lens = (1, q_len, P - 1, P + 1, P + q_len, 2 * P + 7, 650)
+    w = mq("mq_pnb", q_len, G, lens, bs=bs, P=P, seed=6500 + q_len + G + bs + P)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
 def test_mq_single_token_matches_the_single_query_entry():
     import paged_kv_decode_v2_gb300 as pa
     inp = wl.make_inputs(wl.TINY, device="cuda")

@@ -82,6 +82,21 @@ def test_fuzz_block_size_64(dtype, G, P):
     full_check(wl.make_inputs(w, device="cuda"), P)
 
 
+@pytest.mark.parametrize("bs,P", [(16, 300), (32, 200), (64, 100), (16, 8), (32, 48), (64, 1000),
+                                  (16, 17), (32, 1)])
+@pytest.mark.parametrize("G", [4, 16])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_partition_not_a_multiple_of_block_size(bs, P, G, dtype):
+    """Partitions that begin and end inside a block: a straddling block is read
+    by both partitions, each keeping only its own tokens."""
+    lens = sorted({1, bs - 1, bs + 1, P - 1 or 1, P, P + 1, 2 * P + 3, 3 * P + bs + 5, 700})
+    if P < 8:  # keep the partition count (and the oracle's work) small
+        lens = [1, 2, 3, bs + 1, 40]
+    w = wl.Workload("fuzz_pnb", len(lens), 2 * G, 2, 128, bs, P, dtype, "list", seq_lens=tuple(lens),
+                    seed=7000 + bs + P + G + dtype)
+    full_check(wl.make_inputs(w, device="cuda"), P)
+
+
 @pytest.mark.parametrize("D", [64, 256])
 @pytest.mark.parametrize("warps,stages", [(1, 1), (2, 2), (8, 1), (3, 3)])
 def test_launch_shapes_other_head_dims(cuda_lib, D, warps, stages):
