@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
 
     // Visible tokens of this lane's columns 8j + 2t4 (+1): position t - tok0 = lo + r
     // with r < vis: new token i sees positions <= L - q_len + i, and none
-    // before tokA.  Padding columns (past ncols) keep the whole range and are
-    // never stored.
+    // outside the range [tokA, tok0 + ntok) (a straddling block also holds
+    // tokens of the neighbouring partitions).  Padding columns (past ncols)
+    // keep the whole range and are never stored.
     unsigned vis[NT][2];
 #pragma unroll
     for (int j = 0; j < NT; ++j)
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         for (int k = 0; k < 2; ++k) {
             const int n = j * 8 + 2 * t4 + k;
             const int last = (n < ncols ? L - p.q_len + (col0 + n) / p.group : L - 1) - tok0;
-            vis[j][k] = (unsigned)max(last - lo + 1, 0);
+            vis[j][k] = (unsigned)max(min(last + 1, ntok) - lo, 0);
         }
 
     const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
