@@ -51,7 +51,7 @@
  * Supported shapes: head_dim 64, 128 or 256; block_size 16, 32 or 64;
  * partition_size any positive value (a partition may begin or end inside a
  * block; a block that straddles two partitions is read by both); G = num_heads /
- * num_kv_heads an integer in [1, 64]; q_len in [1, 64] with num_seqs *
+ * num_kv_heads an integer in [1, 64]; q_len in [1, 4096] with num_seqs *
  * q_len <= 65535 (the _mq entry points).  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned
  * (they are read with the Tensor Memory Accelerator); query and out 4-byte
@@ -185,8 +185,13 @@ PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_he
  * A partition holding none of the tokens a query sees is written as
  * max_logits = -inf, exp_sums = 0, tmp_output = 0 and adds nothing to the
  * merge.  The K/V cache is read once per call for all q_len * G query rows
- * of a KV head; beyond 16 rows the rows are split over CTAs that run side
- * by side, so their reads meet in L2.  q_len = 1 is pa_decode_v2 / _v1.
+ * of a KV head: up to 31 rows an mma.sync kernel serves 16 rows per CTA,
+ * from 32 rows a tcgen05 kernel serves 128 rows per CTA (see
+ * pa_set_rows_kernel); CTAs that split the rows of one range run side by
+ * side, so their reads meet in L2.  Chunked prefill is this call with q_len
+ * the chunk length, the chunk's own K/V already written to the cache (it
+ * attends to the prefix and causally to itself).  q_len = 1 is
+ * pa_decode_v2 / _v1.
  */
 PA_API int pa_decode_v2_mq(const void *query, const void *key_cache, const void *value_cache,
                            const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
@@ -240,6 +245,20 @@ PA_API int pa_decode(const void *query, const void *key_cache, const void *value
  * Returns PA_ERR_INVALID_ARG for out-of-range values.
  */
 PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
+
+/*
+ * Kernel choice for the query rows of a KV head (rows = q_len * G),
+ * process-wide: 0 (default) picks by row count -- up to 31 rows the
+ * mma.sync kernel (16 rows per CTA), from 32 rows the tcgen05 kernel (128
+ * rows per CTA, S and O accumulated in tensor memory); 1 always the mma.sync
+ * kernel; 2 always the tcgen05 kernel.  Either kernel computes the same
+ * result within the stated tolerances; the choice changes only speed.  The
+ * tcgen05 kernel takes its K/V ring stages from pa_set_launch_config's
+ * stages_per_warp when that is set (at least 2).  Returns PA_ERR_INVALID_ARG for other
+ * values.  There is no counterpart in the method's description: this is a
+ * tuning and test hook.
+ */
+PA_API int pa_set_rows_kernel(int mode);
 
 /*
  * Size of the intermediates array that pa_decode_v2_static keeps inside the

@@ -74,6 +74,8 @@ def load() -> ctypes.CDLL:
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_launch_config.argtypes = [I, I]
     lib.pa_set_launch_config.restype = I
+    lib.pa_set_rows_kernel.argtypes = [I]
+    lib.pa_set_rows_kernel.restype = I
     lib.pa_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P]
     lib.pa_selftest_wait_timeout.restype = I
     _lib = lib
@@ -235,6 +237,11 @@ def pa_decode_choose(num_seqs: int, num_kv_heads: int, max_seq_len: int, partiti
 
 def pa_set_launch_config(warps_per_cta: int = 0, stages_per_warp: int = 0) -> None:
     _check("pa_set_launch_config", load().pa_set_launch_config(warps_per_cta, stages_per_warp))
+
+
+def pa_set_rows_kernel(mode: int = 0) -> None:
+    """0: pick the attention kernel by query rows per KV head; 1: always mma.sync; 2: always tcgen05."""
+    _check("pa_set_rows_kernel", load().pa_set_rows_kernel(mode))
 
 
 def pa_selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:

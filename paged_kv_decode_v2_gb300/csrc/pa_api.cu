@@ -19,6 +19,12 @@ constexpr int kMaxDevices = 64;
 
 std::atomic<int> g_tune_warps{0};
 std::atomic<int> g_tune_stages{0};
+// Kernel for the query rows of a KV head: 0 = by row count, 1 = always the
+// mma.sync kernel, 2 = always the tcgen05 kernel.
+std::atomic<int> g_rows_kernel{0};
+// From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
+// (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
+constexpr int kTcMinRows = 32;
 
 // Per-device cached multiprocessor count (0 = not queried yet).
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -268,11 +274,52 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
     L.smem_bytes = attn_smem(L, warps, stages);
 }
 
+// Per-device dynamic shared memory limit of each tcgen05 kernel after the opt-in.
+constexpr int kTcSlots = 2 * 3 * 3 * 2;
+std::atomic<int> g_tc_smem_limit[kMaxDevices][kTcSlots];
+
+int tc_slot(int dtype, int head_dim, int block_size, bool v1)
+{
+    const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
+    const int bi = block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
+    return (((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (v1 ? 1 : 0);
+}
+
+// The tcgen05 kernel: K/V ring stages as many as keep two CTAs per SM for
+// head_dim <= 128 (four for 64 dims, two for 128) and two for 256 dims; at
+// least two, since S of the next tile is computed while P.V of the current
+// one waits for its softmax.
+int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
+{
+    const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1);
+    size_t limit = (size_t)g_tc_smem_limit[dev][slot].load(std::memory_order_acquire);
+    if (limit == 0) {
+        int optin = 0;
+        if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (tc_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.v1, optin, &limit) != cudaSuccess)
+            return PA_ERR_CUDA;
+        g_tc_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
+    }
+    const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
+    int stages = tune_s > 1 ? tune_s : (tune_s == 1 ? 2 : (L.head_dim == 64 ? 4 : 2));
+    while (stages > 2 && tc_smem_bytes(L.head_dim, stages) > limit)
+        --stages;
+    if (tc_smem_bytes(L.head_dim, stages) > limit)
+        return PA_ERR_UNSUPPORTED;
+    L.p.stages = stages;
+    L.warps = kTcThreads / 32;
+    L.smem_bytes = tc_smem_bytes(L.head_dim, stages);
+    return tc_ops(L.dtype, L.head_dim)->launch(L, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
 {
     int dev;
     if (current_device(&dev))
         return PA_ERR_CUDA;
+    if (L.tc)
+        return prepare_and_launch_tc(L, dev, stream);
     const int sms = sm_count(dev);
     if (sms <= 0)
         return PA_ERR_CUDA;
@@ -314,9 +361,17 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.group = num_heads / num_kv_heads;
     p.q_len = q_len;
     p.cols = p.group * q_len;
-    // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
-    L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
-    p.col_groups = (p.cols + L.cta_cols - 1) / L.cta_cols;
+    const int mode = g_rows_kernel.load(std::memory_order_relaxed);
+    L.tc = mode == 2 || (mode == 0 && p.cols >= kTcMinRows);
+    if (L.tc) {
+        // 128 rows per CTA; the CTAs of one range split the rows.
+        L.cta_cols = kMaxGroup;
+        p.col_groups = (p.cols + kTcRows - 1) / kTcRows;
+    } else {
+        // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
+        L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
+        p.col_groups = (p.cols + L.cta_cols - 1) / L.cta_cols;
+    }
     p.num_blocks = num_blocks;
     p.max_blocks = max_blocks_per_seq;
     p.seq_len_cap = cap;
@@ -625,6 +680,14 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp)
         return PA_ERR_INVALID_ARG;
     g_tune_warps.store(warps_per_cta, std::memory_order_relaxed);
     g_tune_stages.store(stages_per_warp, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+PA_API int pa_set_rows_kernel(int mode)
+{
+    if (mode < 0 || mode > 2)
+        return PA_ERR_INVALID_ARG;
+    g_rows_kernel.store(mode, std::memory_order_relaxed);
     return PA_OK;
 }
 

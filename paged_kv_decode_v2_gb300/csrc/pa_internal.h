@@ -11,11 +11,14 @@
 namespace pa {
 
 constexpr int kMaxGroup = 16;        // query rows (columns) one attention CTA serves
-constexpr int kMaxQLen = 64;         // new tokens per sequence
+constexpr int kMaxQLen = 4096;       // new tokens per sequence
 constexpr int kMaxGQA = 64;          // query heads per KV head
 constexpr int kMaxWarps = 8;         // warps per attention CTA
 constexpr int kMaxStages = 8;        // TMA ring stages per warp
 constexpr int kMergeThreads = 128;   // phase-2 CTA size
+constexpr int kTcRows = 128;         // tcgen05 kernel: query rows per CTA (the MMA's M)
+constexpr int kTcTok = 64;           // tcgen05 kernel: tokens per K/V tile
+constexpr int kTcThreads = 192;      // tcgen05 kernel: 4 row warps, MMA warp, TMA warp
 
 // Arguments of the attention kernel (phase 1 of V2, or V1).
 struct AttnParams {
@@ -50,6 +53,7 @@ struct AttnLaunch {
     int block_size;              // 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
+    bool tc;                     // the tcgen05 kernel (128 query rows per CTA)
     int cta_cols;                // query rows one CTA serves (<= 16): picks the n-tile count
     dim3 grid;
     int warps;
@@ -105,6 +109,34 @@ inline const AttnOps *attn_ops(int dtype, int head_dim)
                                                                        : attn_ops_bf16_d256();
     return head_dim == 64 ? attn_ops_f16_d64() : head_dim == 128 ? attn_ops_f16_d128()
                                                                   : attn_ops_f16_d256();
+}
+
+// Dynamic shared memory of the tcgen05 kernel: the Q tile, `stages` K and V
+// tiles, and 1 KB to align the base to the 1024-byte swizzle atom.
+inline size_t tc_smem_bytes(int head_dim, int stages)
+{
+    return 1024 + (size_t)kTcRows * head_dim * 2 + (size_t)stages * 2 * kTcTok * head_dim * 2;
+}
+
+// Entry points of the tcgen05 attention kernels for one (storage type, head_dim).
+struct TcOps {
+    cudaError_t (*prepare)(int block_size, bool v1, int optin_bytes, size_t *limit);
+    cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
+};
+const TcOps *tc_ops_f16_d64();
+const TcOps *tc_ops_f16_d128();
+const TcOps *tc_ops_f16_d256();
+const TcOps *tc_ops_bf16_d64();
+const TcOps *tc_ops_bf16_d128();
+const TcOps *tc_ops_bf16_d256();
+
+inline const TcOps *tc_ops(int dtype, int head_dim)
+{
+    if (dtype == PA_BF16)
+        return head_dim == 64 ? tc_ops_bf16_d64() : head_dim == 128 ? tc_ops_bf16_d128()
+                                                                     : tc_ops_bf16_d256();
+    return head_dim == 64 ? tc_ops_f16_d64() : head_dim == 128 ? tc_ops_f16_d128()
+                                                                : tc_ops_f16_d256();
 }
 
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,

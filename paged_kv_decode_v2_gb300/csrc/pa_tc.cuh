@@ -1,0 +1,520 @@
+// pa_tc.cuh -- paged attention for many query rows per KV head on the
+// tcgen05 tensor cores: several new tokens per sequence (checking speculated
+// tokens) up to chunked prefill, where a chunk of new tokens attends to the
+// cached prefix and, causally, to itself.
+//
+// Paged-attention pages, "PagedAttention V2" and its split-K description:
+// phase 1 computes, per (sequence, KV head, partition), the softmax
+// statistics and the partition-normalised softmax.V of every query row of
+// the GQA group; phase 2 (pa_merge.cu) merges partitions by log-sum-exp.
+// The same kernel also runs as V1 (one range covering the whole sequence,
+// final output written directly).  The pages' kernels tile
+// [kv_head, gqa, q_len, tile]; this one takes 128 query rows (new token i,
+// head g of the group, row = i * group + g) per CTA as the M of the MMA:
+//
+//   S   = Q K_t^T         tcgen05.mma, M = 128 rows, N = 64 tokens, K = D;
+//                         A = Q and B = K tile in shared memory, S in TMEM
+//   P   = exp(S - m)      one thread per row reads its S row from TMEM,
+//                         masks, keeps the running max m and sum l, and
+//                         writes P (16-bit, split into hi + lo for bf16)
+//                         back to TMEM
+//   O  += P V_t           tcgen05.mma, M = 128, N = D, K = 64 tokens; A = P
+//                         in TMEM, B = V tile (MN-major) in shared memory,
+//                         O in TMEM; rescaled in place when m grows
+//
+// Warp roles: warps 0-3 own the 128 rows (softmax, epilogue), warp 4 issues
+// the MMAs (one thread) and owns the TMEM allocation, warp 5 gathers the K/V
+// blocks of each 64-token tile with TMA into a ring of `stages` stages.
+#pragma once
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+#include "pa_tcgen05.cuh"
+
+namespace pa {
+
+template <int D>
+struct TcCfg {
+    static constexpr int kSlices = D / 64;                          // 128-byte swizzled column slices
+    static constexpr uint32_t kQSlice = kTcRows * 128;              // bytes of one Q slice
+    static constexpr uint32_t kKVSlice = kTcTok * 128;              // bytes of one K or V slice
+    static constexpr uint32_t kQBytes = kQSlice * kSlices;
+    static constexpr uint32_t kKVBytes = kKVSlice * kSlices;        // one K (or V) tile
+    // TMEM columns: O at [0, D), S at [D, D + 64), P hi at [D + 64, D + 96)
+    // and P lo at [D + 96, D + 128) (two 16-bit values per column).
+    static constexpr uint32_t kSCol = D;
+    static constexpr uint32_t kPCol = D + kTcTok;
+    static constexpr uint32_t kCols = D + 2 * kTcTok <= 256 ? 256 : 512;
+};
+
+template <typename T, int D, int BS, bool V1>
+__global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
+    tc_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
+{
+    using C = TcCfg<D>;
+    using E = Elem<T>;
+    constexpr bool kBf16 = E::kSplitP;
+    constexpr int kBPT = kTcTok / BS; // blocks per tile
+
+    __shared__ uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
+    __shared__ uint64_t q_full, s_full, s_free, p_full, o_done, drained;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int abort_sh;
+    extern __shared__ uint8_t dyn_smem[];
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int rt = V1 ? (int)blockIdx.x : (int)blockIdx.x % p.col_groups; // row tile
+    const int part = V1 ? 0 : (int)blockIdx.x / p.col_groups;
+    const int kv = blockIdx.y;
+    const int b = blockIdx.z;
+
+    // Programmatic stream serialisation: nothing global is touched before
+    // the previous grid in the stream has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    int L = __ldg(&p.seq_lens[b]);
+    if (L < 0 || L > p.seq_len_cap) {
+        if (threadIdx.x == 0 && part == 0 && kv == 0 && rt == 0)
+            set_status(p.status, PA_STATUS_BAD_SEQ_LEN);
+        L = L < 0 ? 0 : p.seq_len_cap;
+    }
+    const int tokA = V1 ? 0 : part * p.partition_size;
+    if (!V1 && tokA >= L)
+        return; // partition past the end of the sequence: nothing to write
+
+    // Rows [c0, c0 + nrows) of the KV head's cols = q_len * group rows.
+    const int c0 = rt * kTcRows;
+    const int nrows = min(kTcRows, p.cols - c0);
+    const int i_last = (c0 + nrows - 1) / p.group;
+    // Tokens the CTA needs: [tokA, tokE), the range cut by the causal limit
+    // of its last new token (new token i sees positions <= L - q_len + i).
+    long long e = V1 ? (long long)L : min((long long)L, (long long)tokA + p.partition_size);
+    e = min(e, (long long)L - p.q_len + i_last + 1);
+    const int tokE = (int)e;
+    const int blk0 = tokA / BS;
+    const int tok0 = blk0 * BS;
+    const int ntiles = tokE > tokA ? (tokE - tok0 + kTcTok - 1) / kTcTok : 0;
+    const int nblk = tokE > tokA ? (tokE - tok0 + BS - 1) / BS : 0;
+
+    // This thread's row (warps 0-3).
+    const int r = threadIdx.x;
+    const bool row_ok = r < kTcRows && r < nrows;
+    const int ci = c0 + (row_ok ? r : 0);
+    const int qi = ci / p.group;                 // new token
+    const int head = kv * p.group + ci % p.group;
+    const size_t qrow = ((size_t)b * p.q_len + qi) * p.num_heads + head;
+
+    if (ntiles == 0) {
+        // No row sees a token of the range: an empty partition (m = -inf,
+        // l = 0, o = 0), or a zero output in V1.
+        if (row_ok) {
+            if (V1) {
+                T *out = static_cast<T *>(p.out) + qrow * D;
+                for (int d = 0; d < D; ++d)
+                    out[d] = E::from_float(0.f);
+            } else {
+                const size_t slot = qrow * p.max_num_partitions + part;
+                float4 *tmp = reinterpret_cast<float4 *>(p.tmp_output + slot * D);
+                for (int d = 0; d < D / 4; ++d)
+                    tmp[d] = make_float4(0.f, 0.f, 0.f, 0.f);
+                p.exp_sums[slot] = 0.f;
+                p.max_logits[slot] = -INFINITY;
+            }
+        }
+        return;
+    }
+
+    const int stages = p.stages;
+    const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
+    const uint32_t q_sm = smem0;
+    const uint32_t k_sm = smem0 + C::kQBytes;
+    const uint32_t v_sm = k_sm + (uint32_t)stages * C::kKVBytes;
+    const uint32_t b_k_full = smem_addr(k_full), b_v_full = smem_addr(v_full);
+    const uint32_t b_kv_empty = smem_addr(kv_empty);
+    const uint32_t b_q_full = smem_addr(&q_full), b_s_full = smem_addr(&s_full);
+    const uint32_t b_s_free = smem_addr(&s_free), b_p_full = smem_addr(&p_full);
+    const uint32_t b_o_done = smem_addr(&o_done), b_drained = smem_addr(&drained);
+    volatile int *abort_flag = &abort_sh;
+
+    if (warp == 4) {
+        tmem_alloc(smem_addr(&tmem_base_sh), C::kCols);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 160) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(b_k_full + 8 * s, 1);
+            mbar_init(b_v_full + 8 * s, 1);
+            mbar_init(b_kv_empty + 8 * s, 1);
+        }
+        mbar_init(b_q_full, kTcRows);
+        mbar_init(b_s_full, 1);
+        mbar_init(b_s_free, kTcRows);
+        mbar_init(b_p_full, kTcRows);
+        mbar_init(b_o_done, 1);
+        mbar_init(b_drained, 1);
+        abort_sh = 0;
+        mbar_init_fence();
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+    int32_t status_bits = 0;
+
+    if (warp == 5) {
+        // ---------------------------------------------------------- producer
+        const uint64_t policy = p.col_groups == 1 ? l2_evict_first_policy() : l2_evict_normal_policy();
+        const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks + blk0;
+        int issued = 0;
+        for (int t = 0; t < ntiles; ++t) {
+            const int s = t % stages;
+            const int bi = t * kBPT + lane;
+            int32_t id = 0;
+            if (lane < kBPT && bi < nblk) {
+                id = __ldg(bt + bi);
+                if (id < 0 || id >= p.num_blocks) {
+                    status_bits |= PA_STATUS_BAD_BLOCK_ID;
+                    id = 0; // read a valid block instead of memory outside the cache
+                }
+            }
+            const int nb = min(kBPT, nblk - t * kBPT);
+            // (warp-uniform decision: the loop below shuffles across the warp)
+            if (t >= stages &&
+                !__all_sync(0xffffffffu, mbar_wait_abortable(b_kv_empty + 8 * s,
+                                                             (uint32_t)((t / stages) - 1) & 1u,
+                                                             abort_flag))) {
+                status_bits |= PA_STATUS_TIMEOUT;
+                *abort_flag = 1;
+                break;
+            }
+            const uint32_t bytes = (uint32_t)nb * BS * 128u * C::kSlices;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(b_k_full + 8 * s, bytes);
+                mbar_arrive_expect_tx(b_v_full + 8 * s, bytes);
+            }
+            for (int k = 0; k < nb; ++k) {
+                const int phys = __shfl_sync(0xffffffffu, id, k);
+                if (lane == 0) {
+                    const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
+#pragma unroll
+                    for (int sl = 0; sl < C::kSlices; ++sl) {
+                        const uint32_t off = s * C::kKVBytes + sl * C::kKVSlice + k * BS * 128;
+                        tma_load_3d(k_sm + off, &tmap_k, 0, sl, row, b_k_full + 8 * s, policy);
+                        tma_load_3d(v_sm + off, &tmap_v, 0, sl, row, b_v_full + 8 * s, policy);
+                    }
+                }
+            }
+            issued = t + 1;
+        }
+        // Let copies still in flight land before the CTA's shared memory is
+        // released (they have normally been consumed long ago).
+        for (int t = max(0, issued - stages); t < issued; ++t) {
+            const int s = t % stages;
+            const uint32_t par = (uint32_t)(t / stages) & 1u;
+            mbar_wait_bounded(b_k_full + 8 * s, par, kWaitLimitNs);
+            mbar_wait_bounded(b_v_full + 8 * s, par, kWaitLimitNs);
+        }
+    } else if (warp == 4) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16<kBf16>(kTcRows, kTcTok, false);
+            constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
+            auto issue_s = [&](int t) {
+                const uint32_t kb = k_sm + (uint32_t)(t % stages) * C::kKVBytes;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t sl = ks >> 2, kk = (ks & 3) * 32;
+                    tc_mma_ss(tmem + C::kSCol, smem_desc_sw128(q_sm + sl * C::kQSlice + kk, 16, 1024),
+                              smem_desc_sw128(kb + sl * C::kKVSlice + kk, 16, 1024), idesc_s,
+                              ks > 0);
+                }
+                tc_commit(b_s_full);
+            };
+            bool ok = mbar_wait_abortable(b_q_full, 0, abort_flag) &&
+                      mbar_wait_abortable(b_k_full, 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int t = 0; ok && t < ntiles; ++t) {
+                const int s = t % stages;
+                if (t + 1 < ntiles) {
+                    const int s1 = (t + 1) % stages;
+                    ok = mbar_wait_abortable(b_s_free, (uint32_t)t & 1u, abort_flag) &&
+                         mbar_wait_abortable(b_k_full + 8 * s1, (uint32_t)((t + 1) / stages) & 1u,
+                                             abort_flag);
+                    if (!ok)
+                        break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                }
+                ok = mbar_wait_abortable(b_p_full, (uint32_t)t & 1u, abort_flag) &&
+                     mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / stages) & 1u, abort_flag);
+                if (!ok)
+                    break;
+                tc_fence_after();
+                const uint32_t vb = v_sm + (uint32_t)s * C::kKVBytes;
+#pragma unroll
+                for (int kt = 0; kt < kTcTok / 16; ++kt)
+                    tc_mma_ts(tmem, tmem + C::kPCol + kt * 8,
+                              smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024), idesc_o,
+                              (t > 0 || kt > 0) ? 1u : 0u);
+                if (kBf16) {
+#pragma unroll
+                    for (int kt = 0; kt < kTcTok / 16; ++kt)
+                        tc_mma_ts(tmem, tmem + C::kPCol + 32 + kt * 8,
+                                  smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024), idesc_o, 1u);
+                }
+                tc_commit(b_o_done);
+                tc_commit(b_kv_empty + 8 * s);
+            }
+            if (!ok) {
+                status_bits |= PA_STATUS_TIMEOUT;
+                *abort_flag = 1;
+            }
+            // Every MMA issued has completed once this commit arrives.
+            tc_commit(b_drained);
+            mbar_wait_bounded(b_drained, 0, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------- rows
+        // Q row -> shared memory, 128-byte swizzled (16-byte chunk c of a row
+        // of 64 dims at (c ^ (row & 7)) * 16), zero for padding rows.
+        {
+            const uint32_t *q32 = static_cast<const uint32_t *>(p.query) + qrow * (D / 2);
+#pragma unroll 4
+            for (int ch = 0; ch < D / 8; ++ch) {
+                uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
+                if (row_ok) {
+                    w0 = __ldg(q32 + ch * 4 + 0);
+                    w1 = __ldg(q32 + ch * 4 + 1);
+                    w2 = __ldg(q32 + ch * 4 + 2);
+                    w3 = __ldg(q32 + ch * 4 + 3);
+                }
+                const uint32_t addr =
+                    q_sm + (ch >> 3) * C::kQSlice + r * 128 + ((((ch & 7) ^ (r & 7))) << 4);
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0),
+                             "r"(w1), "r"(w2), "r"(w3)
+                             : "memory");
+            }
+            fence_proxy_async();
+            mbar_arrive(b_q_full);
+        }
+        // Visible tokens of this row: tokA <= t < hi (unsigned span from tokA).
+        const int hi = row_ok ? min(tokE, L - p.q_len + qi + 1) : tokA;
+        const unsigned span = (unsigned)max(hi - tokA, 0);
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const float scale = p.scale;
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            // Waits end in a warp-uniform decision: tcgen05.ld / st are warp-collective.
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full, (uint32_t)t & 1u, abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[2][32];
+            tmem_ld32(lane_base + C::kSCol, sr[0]);
+            tmem_ld32(lane_base + C::kSCol + 32, sr[1]);
+            tc_fence_before();
+            mbar_arrive(b_s_free);
+
+            const int off = tok0 + t * kTcTok - tokA; // token (t's first) - tokA
+            float sv[kTcTok];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTcTok; ++c) {
+                const float s = __uint_as_float(sr[c >> 5][c & 31]);
+                sv[c] = (unsigned)(off + c) < span ? s * scale : -INFINITY;
+                mx = fmaxf(mx, sv[c]);
+            }
+            const float mn = fmaxf(m_run, mx);
+            // A row with no visible token yet (max still -inf) keeps l = o = 0.
+            const float a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
+            const float mb = mn != -INFINITY ? mn * kLog2e : 0.f;
+            uint32_t ph[32], pl[32];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTcTok; c += 2) {
+                const float p0 = fast_exp2(fmaf(sv[c], kLog2e, -mb));
+                const float p1 = fast_exp2(fmaf(sv[c + 1], kLog2e, -mb));
+                lsum += p0 + p1;
+                const uint32_t h = E::pack(p0, p1);
+                ph[c >> 1] = h;
+                pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
+            }
+            l_run = fmaf(l_run, a, lsum);
+            m_run = mn;
+
+            // O and the P columns are free once the previous P.V has completed.
+            if (t > 0) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_abortable(b_o_done, (uint32_t)(t - 1) & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, a != 1.f)) {
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + cc, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
+                        tmem_st32(lane_base + cc, o);
+                    }
+                }
+            }
+            tmem_st32(lane_base + C::kPCol, ph);
+            if (kBf16)
+                tmem_st32(lane_base + C::kPCol + 32, pl);
+
+            if (t == ntiles - 1) {
+                // Tile rows past the range (unloaded blocks, slots past the
+                // sequence end) may hold anything: zero them in V so that
+                // 0 * garbage cannot reach O.
+                const int vt = tokE - (tok0 + t * kTcTok);
+                if (vt < kTcTok) {
+                    const int s = t % stages;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / stages) & 1u,
+                                                        abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t vb = v_sm + (uint32_t)s * C::kKVBytes;
+                    const int nchunks = (kTcTok - vt) * 8 * C::kSlices;
+                    for (int idx = r; idx < nchunks; idx += kTcRows) {
+                        const int sl = idx % C::kSlices;
+                        const int rest = idx / C::kSlices;
+                        st_shared_zero16(vb + sl * C::kKVSlice + (vt + rest / 8) * 128 + (rest & 7) * 16);
+                    }
+                    fence_proxy_async();
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(b_p_full);
+        }
+        if (ok && !__all_sync(0xffffffffu, mbar_wait_abortable(b_o_done, (uint32_t)(ntiles - 1) & 1u,
+                                                               abort_flag)))
+            ok = false;
+        if (!ok) {
+            status_bits |= PA_STATUS_TIMEOUT;
+            *abort_flag = 1;
+        } else {
+            tc_fence_after();
+            // ---- epilogue: O / l for the row
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            if (V1) {
+                uint32_t *out = reinterpret_cast<uint32_t *>(static_cast<T *>(p.out) + qrow * D);
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + cc, o);
+                    if (row_ok) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2)
+                            out[(cc + k) / 2] = E::pack(__uint_as_float(o[k]) * inv,
+                                                        __uint_as_float(o[k + 1]) * inv);
+                    }
+                }
+            } else {
+                const size_t slot = qrow * p.max_num_partitions + part;
+                float4 *tmp = reinterpret_cast<float4 *>(p.tmp_output + slot * D);
+#pragma unroll 1
+                for (int cc = 0; cc < D; cc += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + cc, o);
+                    if (row_ok) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 4)
+                            tmp[(cc + k) / 4] = make_float4(
+                                __uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                                __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                    }
+                }
+                if (row_ok) {
+                    p.exp_sums[slot] = l_run;
+                    p.max_logits[slot] = m_run;
+                }
+            }
+        }
+    }
+
+    if (status_bits)
+        set_status(p.status, status_bits);
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kCols);
+    }
+}
+
+template <typename T, int D>
+static const void *tc_kernel_ptr(int block_size, bool v1)
+{
+#define PA_PICK(BS)                                                                               \
+    if (block_size == BS)                                                                         \
+        return v1 ? reinterpret_cast<const void *>(&tc_attn_kernel<T, D, BS, true>)               \
+                  : reinterpret_cast<const void *>(&tc_attn_kernel<T, D, BS, false>);
+    PA_PICK(16)
+    PA_PICK(32)
+    PA_PICK(64)
+#undef PA_PICK
+    return nullptr;
+}
+
+template <typename T, int D>
+static cudaError_t tc_prepare(int block_size, bool v1, int optin_bytes, size_t *limit)
+{
+    const void *fn = tc_kernel_ptr<T, D>(block_size, v1);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess)
+        return e;
+    if ((size_t)optin_bytes <= fa.sharedSizeBytes)
+        return cudaErrorInvalidValue;
+    *limit = (size_t)optin_bytes - fa.sharedSizeBytes;
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*limit);
+}
+
+template <typename T, int D>
+static cudaError_t tc_launch(const AttnLaunch &L, cudaStream_t stream)
+{
+    const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1);
+    if (!fn)
+        return cudaErrorInvalidValue;
+    void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
+                    const_cast<AttnParams *>(&L.p)};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = L.grid;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = L.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+#define PA_DEFINE_TC_OPS(T, NAME, D)                                                              \
+    const TcOps *NAME()                                                                           \
+    {                                                                                             \
+        static const TcOps ops = {&tc_prepare<T, D>, &tc_launch<T, D>};                           \
+        return &ops;                                                                              \
+    }
+
+} // namespace pa

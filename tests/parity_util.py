@@ -141,3 +141,45 @@ def check_partitions(inp: wl.Inputs, P: int, tmp, es, ml, pairs=None, prob=None)
 def oracle_out(inp: wl.Inputs, pairs=None, prob=None):
     prob = prob or oracle_problem(inp)
     return oracle.decode(prob, pairs=pairs)
+
+
+# ---------------------------------------------------------------- several new tokens per sequence
+
+def run_mq(inp, P, entry="v2", hint=0, status=None):
+    import paged_kv_decode_v2_gb300 as pa
+    w = inp.workload
+    S, Q, H, D = inp.query.shape
+    cap = inp.block_tables.shape[1] * w.block_size
+    if hint > 0:
+        cap = min(cap, hint)
+    npmax = max(1, pa.num_partitions(cap, P))
+    tmp, es, ml = pa.alloc_workspace(S, H, D, npmax, q_len=Q)
+    for t in (tmp, es, ml):
+        t.fill_(float("nan"))
+    out = torch.full_like(inp.query, float("nan"))
+    args = (inp.query, inp.key_cache, inp.value_cache, inp.block_tables, inp.seq_lens, w.scale)
+    if entry == "v2":
+        pa.pa_decode_v2_mq(*args, P, out, tmp, es, ml, max_seq_len_hint=hint, status=status)
+    else:
+        pa.pa_decode_v1_mq(*args, out, max_seq_len_hint=hint, status=status)
+    torch.cuda.synchronize()
+    return out, tmp, es, ml
+
+
+def check_mq(inp, P, entries=("v2", "v1")):
+    prob = oracle_problem(inp)
+    ref = oracle.decode(prob)  # [S, Q, H, D]
+    S, Q, H, D = inp.query.shape
+    for e in entries:
+        out, tmp, es, ml = run_mq(inp, P, entry=e)
+        check_out(out, ref, inp.workload.dtype, what=f"{inp.workload.name}/{e}")
+        if e == "v2":
+            pairs = [(r, h) for r in range(S * Q) for h in range(H)]
+            check_partitions(inp, P, tmp.view(S * Q, H, *tmp.shape[3:]), es.view(S * Q, H, -1),
+                             ml.view(S * Q, H, -1), pairs=pairs, prob=prob)
+    return ref
+
+
+def mq(name, q_len, G, lens, bs=16, P=64, dtype=wl.BF16, D=128, KV=2, seed=0):
+    return wl.Workload(name, len(lens), G * KV, KV, D, bs, P, dtype, "list", seq_lens=tuple(lens),
+                       q_len=q_len, seed=seed)

@@ -23,7 +23,7 @@ def test_header_declares_the_entry_points():
     for n in ("pa_decode_v2", "pa_decode_v1", "pa_decode", "pa_decode_v2_phase1",
               "pa_decode_v2_phase2", "pa_v2_num_partitions", "pa_v2_workspace_bytes",
               "pa_status_string", "pa_decode_choose", "pa_selftest_wait_timeout",
-              "pa_set_launch_config"):
+              "pa_set_launch_config", "pa_set_rows_kernel"):
         assert n in names
 
 
@@ -108,6 +108,14 @@ def test_launch_config_override_validation(cuda_lib):
     assert cuda_lib.load().pa_set_launch_config(9, 2) == 1
     assert cuda_lib.load().pa_set_launch_config(4, 9) == 1
     assert cuda_lib.load().pa_set_launch_config(0, 0) == 0
+
+
+def test_rows_kernel_override_validation(cuda_lib):
+    lib = cuda_lib.load()
+    assert lib.pa_set_rows_kernel(-1) == 1
+    assert lib.pa_set_rows_kernel(3) == 1
+    assert lib.pa_set_rows_kernel(2) == 0
+    assert lib.pa_set_rows_kernel(0) == 0
 
 
 def test_selftest_rejects_bad_limits(cuda_lib):

@@ -1,0 +1,144 @@
+"""GPU parity for the tcgen05 kernel: 128 query rows (new token i, head g of
+the GQA group) per CTA, S = Q K^T and O += P V on the fifth-generation
+tensor cores with S, P and O in tensor memory.
+
+Every test forces that kernel (pa_set_rows_kernel(2)) and compares the CUDA
+path, V2 (partials + merge) and V1, element by element with the fp64 oracle,
+with the tolerances of parity_util: row counts below, at and above one CTA's
+128 rows, every head_dim and block size, K/V tiles that end inside a block,
+partitions that begin inside a block, a ring of one to five stages, chunked
+prefill (a chunk of new tokens attending to a cached prefix and causally to
+itself), poisoned caches and bad block ids.
+"""
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from parity_util import (check_mq, check_out, check_partitions, mq, oracle_problem, run_mq,
+                         run_v2)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _force_tc(cuda_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    cuda_lib.pa_set_launch_config(0, 0)
+    cuda_lib.pa_set_rows_kernel(2)
+    yield
+    cuda_lib.pa_set_rows_kernel(0)
+    cuda_lib.pa_set_launch_config(0, 0)
+
+
+def check_single(inp, P):
+    """q_len = 1 (query [S, H, D]) through pa_decode_v2 and pa_decode_v1."""
+    prob = oracle_problem(inp)
+    ref = oracle.decode(prob)
+    for e in ("v2", "v1"):
+        out, tmp, es, ml = run_v2(inp, P, entry=e)
+        check_out(out, ref, inp.workload.dtype, what=f"{inp.workload.name}/{e}")
+        if e == "v2":
+            check_partitions(inp, P, tmp, es, ml, prob=prob)
+
+
+@pytest.mark.parametrize("q_len,G", [(2, 16), (4, 8), (8, 4), (3, 16), (32, 4), (16, 8), (33, 4)])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_row_counts(q_len, G, dtype):
+    """32 to 132 rows per KV head: padding rows, exactly one CTA, two CTAs."""
+    P = 128
+    lens = (1, q_len, 63, 64, 65, P - 1, P + 1, 2 * P + 70, 700)
+    w = mq("tc_rows", q_len, G, lens, P=P, dtype=dtype, seed=8000 + 31 * q_len + G + dtype)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("G", [1, 8, 64])
+def test_tc_single_query(G):
+    P = 256
+    lens = (1, 64, 255, 257, 1000)
+    w = wl.Workload("tc_q1", len(lens), 2 * G, 2, 128, 16, P, wl.BF16, "list", seq_lens=lens,
+                    seed=8100 + G)
+    check_single(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_head_dims_and_block_sizes(D, bs, dtype):
+    P = 128
+    lens = (5, bs - 1, bs + 1, 130, 333)
+    w = mq("tc_shapes", 4, 8, lens, bs=bs, P=P, D=D, dtype=dtype, seed=8200 + D + bs + dtype)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("stages", [1, 3, 5])
+def test_tc_ring_stages(cuda_lib, stages):
+    """The K/V ring wraps many times (V1 walks 1000+ tokens); a request for
+    one stage runs with two."""
+    cuda_lib.pa_set_launch_config(0, stages)
+    w = mq("tc_stages", 8, 4, (700, 1100, 64), P=256, seed=8300 + stages)
+    check_mq(wl.make_inputs(w, device="cuda"), 256)
+
+
+@pytest.mark.parametrize("bs,P", [(16, 100), (32, 300), (16, 8), (64, 1000)])
+def test_tc_partition_not_a_multiple_of_block_size(bs, P):
+    lens = (1, 8, P - 1, P + 1, 2 * P + 7, 650)
+    w = mq("tc_pnb", 8, 4, lens, bs=bs, P=P, seed=8400 + bs + P)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("q_len,prefix", [(128, 0), (128, 37), (300, 1000), (64, 4000)])
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_chunked_prefill(q_len, prefix, dtype):
+    """A chunk of q_len new tokens whose K/V are already in the cache after a
+    prefix: new token i attends to the prefix and to chunk tokens <= i."""
+    lens = (prefix + q_len, q_len + 5)
+    w = mq("tc_prefill", q_len, 4, lens, P=512, dtype=dtype, seed=8500 + q_len + prefix + dtype)
+    check_mq(wl.make_inputs(w, device="cuda"), 512)
+
+
+def test_tc_agrees_with_the_mma_sync_kernel(cuda_lib):
+    """Both kernels on the same inputs, each against the oracle and against the other."""
+    w = mq("tc_vs_mma", 8, 4, (3, 100, 513, 900), P=256, seed=8600)
+    inp = wl.make_inputs(w, device="cuda")
+    ref = check_mq(inp, 256)
+    tc_out = run_mq(inp, 256)[0]
+    cuda_lib.pa_set_rows_kernel(1)
+    mma_out = run_mq(inp, 256)[0]
+    check_out(mma_out, ref, w.dtype, what="mma.sync")
+    d = (tc_out.float() - mma_out.float()).abs().max().item()
+    assert d <= 2 * 2e-3 + 2 ** -8, d
+
+
+def test_tc_unreferenced_slots_and_relabelling():
+    """Poison never reaches the output; relabelling physical blocks changes nothing (bitwise)."""
+    w = mq("tc_poison", 8, 4, (3, 37, 200, 64), bs=16, P=64, seed=8700)
+    inp = wl.make_inputs(w, device="cuda", max_blocks=20)
+    clean = [run_mq(inp, 64, entry=e)[0] for e in ("v2", "v1")]
+    wl.poison_unreferenced(inp, float("nan"))
+    for a, e in zip(clean, ("v2", "v1")):
+        assert torch.equal(a, run_mq(inp, 64, entry=e)[0])
+    r = wl.relabel_blocks(inp, seed=11)
+    for a, e in zip(clean, ("v2", "v1")):
+        assert torch.equal(a, run_mq(r, 64, entry=e)[0])
+
+
+def test_tc_bad_block_id_sets_status_and_clean_call_does_not():
+    w = mq("tc_status", 8, 4, (100, 300), P=64, seed=8800)
+    inp = wl.make_inputs(w, device="cuda")
+    for e in ("v2", "v1"):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        run_mq(inp, 64, entry=e, status=st)
+        assert int(st.item()) == 0
+    inp.block_tables[1, 3] = inp.key_cache.shape[0] + 1
+    for e in ("v2", "v1"):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        run_mq(inp, 64, entry=e, status=st)
+        assert int(st.item()) & 1
+
+
+def test_tc_speculative_batch_full_size():
+    """Batch decode (32 seqs up to 8192 tokens, 32/8 heads) checking 8 speculated tokens each."""
+    w = wl.BATCH.with_(name="batch_spec8", q_len=8)
+    check_mq(wl.make_inputs(w, device="cuda"), w.partition_size)
