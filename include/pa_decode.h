@@ -185,8 +185,8 @@ PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_he
  * A partition holding none of the tokens a query sees is written as
  * max_logits = -inf, exp_sums = 0, tmp_output = 0 and adds nothing to the
  * merge.  The K/V cache is read once per call for all q_len * G query rows
- * of a KV head: up to 31 rows an mma.sync kernel serves 16 rows per CTA,
- * from 32 rows a tcgen05 kernel serves 128 rows per CTA (see
+ * of a KV head: up to 63 rows an mma.sync kernel serves 16 rows per CTA,
+ * from 64 rows a tcgen05 kernel serves 128 rows per CTA (see
  * pa_set_rows_kernel); CTAs that split the rows of one range run side by
  * side, so their reads meet in L2.  Chunked prefill is this call with q_len
  * the chunk length, the chunk's own K/V already written to the cache (it
@@ -248,13 +248,14 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
 
 /*
  * Kernel choice for the query rows of a KV head (rows = q_len * G),
- * process-wide: 0 (default) picks by row count -- up to 31 rows the
- * mma.sync kernel (16 rows per CTA), from 32 rows the tcgen05 kernel (128
+ * process-wide: 0 (default) picks by row count -- up to 63 rows the
+ * mma.sync kernel (16 rows per CTA), from 64 rows the tcgen05 kernel (128
  * rows per CTA, S and O accumulated in tensor memory); 1 always the mma.sync
  * kernel; 2 always the tcgen05 kernel.  Either kernel computes the same
  * result within the stated tolerances; the choice changes only speed.  The
- * tcgen05 kernel takes its K/V ring stages from pa_set_launch_config's
- * stages_per_warp when that is set (at least 2).  Returns PA_ERR_INVALID_ARG for other
+ * tcgen05 kernel takes its K ring stages from pa_set_launch_config's
+ * stages_per_warp and its V ring stages from warps_per_cta when those are
+ * set.  Returns PA_ERR_INVALID_ARG for other
  * values.  There is no counterpart in the method's description: this is a
  * tuning and test hook.
  */

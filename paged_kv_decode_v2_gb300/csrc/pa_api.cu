@@ -24,7 +24,7 @@ std::atomic<int> g_tune_stages{0};
 std::atomic<int> g_rows_kernel{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
-constexpr int kTcMinRows = 32;
+constexpr int kTcMinRows = 64;
 
 // Per-device cached multiprocessor count (0 = not queried yet).
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -285,10 +285,10 @@ int tc_slot(int dtype, int head_dim, int block_size, bool v1)
     return (((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (v1 ? 1 : 0);
 }
 
-// The tcgen05 kernel: K/V ring stages as many as keep two CTAs per SM for
-// head_dim <= 128 (four for 64 dims, two for 128) and two for 256 dims; at
-// least two, since S of the next tile is computed while P.V of the current
-// one waits for its softmax.
+// The tcgen05 kernel: as many K and V ring stages as keep two CTAs per SM
+// for head_dim <= 128 (one for 256 dims, whose TMEM takes the whole SM).
+// pa_set_launch_config's stages_per_warp overrides the K stages and its
+// warps_per_cta the V stages.
 int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
 {
     const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1);
@@ -302,14 +302,24 @@ int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
         g_tc_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
     }
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
-    int stages = tune_s > 1 ? tune_s : (tune_s == 1 ? 2 : (L.head_dim == 64 ? 4 : 2));
-    while (stages > 2 && tc_smem_bytes(L.head_dim, stages) > limit)
-        --stages;
-    if (tc_smem_bytes(L.head_dim, stages) > limit)
+    const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
+    int ks = L.head_dim == 64 ? 4 : 2, vs = ks;
+    if (tune_s > 0)
+        ks = tune_s;
+    if (tune_w > 0)
+        vs = tune_w;
+    while (tc_smem_bytes(L.head_dim, ks, vs) > limit && (ks > 1 || vs > 1)) {
+        if (ks >= vs)
+            --ks;
+        else
+            --vs;
+    }
+    if (tc_smem_bytes(L.head_dim, ks, vs) > limit)
         return PA_ERR_UNSUPPORTED;
-    L.p.stages = stages;
+    L.p.stages = ks;
+    L.p.v_stages = vs;
     L.warps = kTcThreads / 32;
-    L.smem_bytes = tc_smem_bytes(L.head_dim, stages);
+    L.smem_bytes = tc_smem_bytes(L.head_dim, ks, vs);
     return tc_ops(L.dtype, L.head_dim)->launch(L, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

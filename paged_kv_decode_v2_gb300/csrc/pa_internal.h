@@ -36,7 +36,8 @@ struct AttnParams {
     int seq_len_cap;             // lengths are clamped to [0, cap]
     float scale;
     int partition_size;          // V2: tokens per partition (any positive value)
-    int stages;                  // TMA ring stages per warp
+    int stages;                  // TMA ring stages per warp (tcgen05 kernel: K ring stages)
+    int v_stages;                // tcgen05 kernel: V ring stages
     int max_num_partitions;      // V2: partition capacity of the intermediates
     float *tmp_output;           // V2: [S, q_len, H, NPcap, D]
     float *exp_sums;             // V2: [S, q_len, H, NPcap]
@@ -111,11 +112,13 @@ inline const AttnOps *attn_ops(int dtype, int head_dim)
                                                                   : attn_ops_f16_d256();
 }
 
-// Dynamic shared memory of the tcgen05 kernel: the Q tile, `stages` K and V
-// tiles, and 1 KB to align the base to the 1024-byte swizzle atom.
-inline size_t tc_smem_bytes(int head_dim, int stages)
+// Dynamic shared memory of the tcgen05 kernel: the Q tile, k_stages K tiles
+// and v_stages V tiles, and 1 KB to align the base to the 1024-byte swizzle
+// atom.
+inline size_t tc_smem_bytes(int head_dim, int k_stages, int v_stages)
 {
-    return 1024 + (size_t)kTcRows * head_dim * 2 + (size_t)stages * 2 * kTcTok * head_dim * 2;
+    return 1024 + (size_t)kTcRows * head_dim * 2 +
+           (size_t)(k_stages + v_stages) * kTcTok * head_dim * 2;
 }
 
 // Entry points of the tcgen05 attention kernels for one (storage type, head_dim).

@@ -23,8 +23,9 @@
 //                         O in TMEM; rescaled in place when m grows
 //
 // Warp roles: warps 0-3 own the 128 rows (softmax, epilogue), warp 4 issues
-// the MMAs (one thread) and owns the TMEM allocation, warp 5 gathers the K/V
-// blocks of each 64-token tile with TMA into a ring of `stages` stages.
+// the MMAs (one thread) and owns the TMEM allocation, two lanes of warp 5
+// gather the K and the V blocks of each 64-token tile with TMA, each into its
+// own ring (p.stages K stages, p.v_stages V stages).
 #pragma once
 
 #include "pa_device.cuh"
@@ -57,7 +58,8 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     constexpr bool kBf16 = E::kSplitP;
     constexpr int kBPT = kTcTok / BS; // blocks per tile
 
-    __shared__ uint64_t k_full[kMaxStages], v_full[kMaxStages], kv_empty[kMaxStages];
+    __shared__ uint64_t k_full[kMaxStages], v_full[kMaxStages], k_empty[kMaxStages],
+        v_empty[kMaxStages];
     __shared__ uint64_t q_full, s_full, s_free, p_full, o_done, drained;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
@@ -127,13 +129,14 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
         return;
     }
 
-    const int stages = p.stages;
+    const int kst = p.stages;   // K ring stages
+    const int vst = p.v_stages; // V ring stages
     const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
     const uint32_t q_sm = smem0;
     const uint32_t k_sm = smem0 + C::kQBytes;
-    const uint32_t v_sm = k_sm + (uint32_t)stages * C::kKVBytes;
+    const uint32_t v_sm = k_sm + (uint32_t)kst * C::kKVBytes;
     const uint32_t b_k_full = smem_addr(k_full), b_v_full = smem_addr(v_full);
-    const uint32_t b_kv_empty = smem_addr(kv_empty);
+    const uint32_t b_k_empty = smem_addr(k_empty), b_v_empty = smem_addr(v_empty);
     const uint32_t b_q_full = smem_addr(&q_full), b_s_full = smem_addr(&s_full);
     const uint32_t b_s_free = smem_addr(&s_free), b_p_full = smem_addr(&p_full);
     const uint32_t b_o_done = smem_addr(&o_done), b_drained = smem_addr(&drained);
@@ -144,10 +147,13 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
         tmem_relinquish();
     }
     if (threadIdx.x == 160) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < kst; ++s) {
             mbar_init(b_k_full + 8 * s, 1);
+            mbar_init(b_k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < vst; ++s) {
             mbar_init(b_v_full + 8 * s, 1);
-            mbar_init(b_kv_empty + 8 * s, 1);
+            mbar_init(b_v_empty + 8 * s, 1);
         }
         mbar_init(b_q_full, kTcRows);
         mbar_init(b_s_full, 1);
@@ -167,65 +173,78 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     int32_t status_bits = 0;
 
     if (warp == 5) {
-        // ---------------------------------------------------------- producer
-        const uint64_t policy = p.col_groups == 1 ? l2_evict_first_policy() : l2_evict_normal_policy();
-        const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks + blk0;
-        int issued = 0;
-        for (int t = 0; t < ntiles; ++t) {
-            const int s = t % stages;
-            const int bi = t * kBPT + lane;
-            int32_t id = 0;
-            if (lane < kBPT && bi < nblk) {
-                id = __ldg(bt + bi);
-                if (id < 0 || id >= p.num_blocks) {
-                    status_bits |= PA_STATUS_BAD_BLOCK_ID;
-                    id = 0; // read a valid block instead of memory outside the cache
-                }
-            }
-            const int nb = min(kBPT, nblk - t * kBPT);
-            // (warp-uniform decision: the loop below shuffles across the warp)
-            if (t >= stages &&
-                !__all_sync(0xffffffffu, mbar_wait_abortable(b_kv_empty + 8 * s,
-                                                             (uint32_t)((t / stages) - 1) & 1u,
-                                                             abort_flag))) {
-                status_bits |= PA_STATUS_TIMEOUT;
-                *abort_flag = 1;
-                break;
-            }
-            const uint32_t bytes = (uint32_t)nb * BS * 128u * C::kSlices;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(b_k_full + 8 * s, bytes);
-                mbar_arrive_expect_tx(b_v_full + 8 * s, bytes);
-            }
-            for (int k = 0; k < nb; ++k) {
-                const int phys = __shfl_sync(0xffffffffu, id, k);
-                if (lane == 0) {
-                    const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
+        // ---------------------------------------------------------- producers
+        // Lane 0 loads the K tiles, lane 1 the V tiles, each into its own
+        // ring and at its own pace: a K stage is free again once S of its
+        // tile is computed, a V stage once P.V is.  Block ids are fetched a
+        // tile ahead of their use.
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+            const uint32_t ring = is_k ? k_sm : v_sm;
+            const uint32_t full = is_k ? b_k_full : b_v_full;
+            const uint32_t empty = is_k ? b_k_empty : b_v_empty;
+            const int stages = is_k ? kst : vst;
+            const uint64_t policy =
+                p.col_groups == 1 ? l2_evict_first_policy() : l2_evict_normal_policy();
+            const int32_t *bt = p.block_tables + (size_t)b * p.max_blocks + blk0;
+            int32_t ids[kBPT], nxt[kBPT];
+            auto fetch = [&](int t, int32_t(&dst)[kBPT]) {
 #pragma unroll
-                    for (int sl = 0; sl < C::kSlices; ++sl) {
-                        const uint32_t off = s * C::kKVBytes + sl * C::kKVSlice + k * BS * 128;
-                        tma_load_3d(k_sm + off, &tmap_k, 0, sl, row, b_k_full + 8 * s, policy);
-                        tma_load_3d(v_sm + off, &tmap_v, 0, sl, row, b_v_full + 8 * s, policy);
+                for (int k = 0; k < kBPT; ++k) {
+                    const int bi = t * kBPT + k;
+                    int32_t id = 0;
+                    if (t < ntiles && bi < nblk) {
+                        id = __ldg(bt + bi);
+                        if (id < 0 || id >= p.num_blocks) {
+                            status_bits |= PA_STATUS_BAD_BLOCK_ID;
+                            id = 0; // read a valid block instead of memory outside the cache
+                        }
+                    }
+                    dst[k] = id;
+                }
+            };
+            fetch(0, nxt);
+            int issued = 0;
+            for (int t = 0; t < ntiles; ++t) {
+#pragma unroll
+                for (int k = 0; k < kBPT; ++k)
+                    ids[k] = nxt[k];
+                fetch(t + 1, nxt);
+                const int s = t % stages;
+                if (t >= stages &&
+                    !mbar_wait_abortable(empty + 8 * s, (uint32_t)((t / stages) - 1) & 1u, abort_flag)) {
+                    status_bits |= PA_STATUS_TIMEOUT;
+                    *abort_flag = 1;
+                    break;
+                }
+                const int nb = min(kBPT, nblk - t * kBPT);
+                mbar_arrive_expect_tx(full + 8 * s, (uint32_t)nb * BS * 128u * C::kSlices);
+#pragma unroll
+                for (int k = 0; k < kBPT; ++k) {
+                    if (k < nb) {
+                        const int row = (int)(((long long)ids[k] * p.num_kv_heads + kv) * BS);
+#pragma unroll
+                        for (int sl = 0; sl < C::kSlices; ++sl)
+                            tma_load_3d(ring + s * C::kKVBytes + sl * C::kKVSlice + k * BS * 128, map,
+                                        0, sl, row, full + 8 * s, policy);
                     }
                 }
+                issued = t + 1;
             }
-            issued = t + 1;
+            // Let copies still in flight land before the CTA's shared memory
+            // is released (they have normally been consumed long ago).
+            for (int t = max(0, issued - stages); t < issued; ++t)
+                mbar_wait_bounded(full + 8 * (t % stages), (uint32_t)(t / stages) & 1u, kWaitLimitNs);
         }
-        // Let copies still in flight land before the CTA's shared memory is
-        // released (they have normally been consumed long ago).
-        for (int t = max(0, issued - stages); t < issued; ++t) {
-            const int s = t % stages;
-            const uint32_t par = (uint32_t)(t / stages) & 1u;
-            mbar_wait_bounded(b_k_full + 8 * s, par, kWaitLimitNs);
-            mbar_wait_bounded(b_v_full + 8 * s, par, kWaitLimitNs);
-        }
+        __syncwarp();
     } else if (warp == 4) {
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16<kBf16>(kTcRows, kTcTok, false);
             constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
             auto issue_s = [&](int t) {
-                const uint32_t kb = k_sm + (uint32_t)(t % stages) * C::kKVBytes;
+                const uint32_t kb = k_sm + (uint32_t)(t % kst) * C::kKVBytes;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t sl = ks >> 2, kk = (ks & 3) * 32;
@@ -234,6 +253,7 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                               ks > 0);
                 }
                 tc_commit(b_s_full);
+                tc_commit(b_k_empty + 8 * (t % kst));
             };
             bool ok = mbar_wait_abortable(b_q_full, 0, abort_flag) &&
                       mbar_wait_abortable(b_k_full, 0, abort_flag);
@@ -242,11 +262,11 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 issue_s(0);
             }
             for (int t = 0; ok && t < ntiles; ++t) {
-                const int s = t % stages;
+                const int s = t % vst;
                 if (t + 1 < ntiles) {
-                    const int s1 = (t + 1) % stages;
+                    const int s1 = (t + 1) % kst;
                     ok = mbar_wait_abortable(b_s_free, (uint32_t)t & 1u, abort_flag) &&
-                         mbar_wait_abortable(b_k_full + 8 * s1, (uint32_t)((t + 1) / stages) & 1u,
+                         mbar_wait_abortable(b_k_full + 8 * s1, (uint32_t)((t + 1) / kst) & 1u,
                                              abort_flag);
                     if (!ok)
                         break;
@@ -254,7 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                     issue_s(t + 1);
                 }
                 ok = mbar_wait_abortable(b_p_full, (uint32_t)t & 1u, abort_flag) &&
-                     mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / stages) & 1u, abort_flag);
+                     mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u, abort_flag);
                 if (!ok)
                     break;
                 tc_fence_after();
@@ -271,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                                   smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024), idesc_o, 1u);
                 }
                 tc_commit(b_o_done);
-                tc_commit(b_kv_empty + 8 * s);
+                tc_commit(b_v_empty + 8 * s);
             }
             if (!ok) {
                 status_bits |= PA_STATUS_TIMEOUT;
@@ -288,10 +308,18 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
         // of 64 dims at (c ^ (row & 7)) * 16), zero for padding rows.
         {
             const uint32_t *q32 = static_cast<const uint32_t *>(p.query) + qrow * (D / 2);
+            // Rows are D * 2 bytes apart, so one base check covers every row.
+            const bool vec = (reinterpret_cast<uintptr_t>(p.query) & 15u) == 0;
 #pragma unroll 4
             for (int ch = 0; ch < D / 8; ++ch) {
                 uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-                if (row_ok) {
+                if (row_ok && vec) {
+                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q32) + ch);
+                    w0 = v.x;
+                    w1 = v.y;
+                    w2 = v.z;
+                    w3 = v.w;
+                } else if (row_ok) {
                     w0 = __ldg(q32 + ch * 4 + 0);
                     w1 = __ldg(q32 + ch * 4 + 1);
                     w2 = __ldg(q32 + ch * 4 + 2);
@@ -327,29 +355,47 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             mbar_arrive(b_s_free);
 
             const int off = tok0 + t * kTcTok - tokA; // token (t's first) - tokA
-            float sv[kTcTok];
-            float mx = -INFINITY;
+            // x: the exp2 argument is x * cf - mb.  On a tile every row of the
+            // warp sees whole (the common case) with scale > 0, x is the raw
+            // score and the scale folds into cf (max(s) * scale = max(s * scale)
+            // for scale > 0); otherwise x = s * scale, or -inf where masked.
+            float x[kTcTok];
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}; // independent chains
+            float mx, cf;
+            if (__all_sync(0xffffffffu, scale > 0.f && off >= 0 && off + kTcTok <= (int)span)) {
 #pragma unroll
-            for (int c = 0; c < kTcTok; ++c) {
-                const float s = __uint_as_float(sr[c >> 5][c & 31]);
-                sv[c] = (unsigned)(off + c) < span ? s * scale : -INFINITY;
-                mx = fmaxf(mx, sv[c]);
+                for (int c = 0; c < kTcTok; ++c) {
+                    x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                }
+                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale;
+                cf = scale * kLog2e;
+            } else {
+#pragma unroll
+                for (int c = 0; c < kTcTok; ++c) {
+                    const float s = __uint_as_float(sr[c >> 5][c & 31]);
+                    x[c] = (unsigned)(off + c) < span ? s * scale : -INFINITY;
+                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                }
+                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                cf = kLog2e;
             }
             const float mn = fmaxf(m_run, mx);
             // A row with no visible token yet (max still -inf) keeps l = o = 0.
             const float a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
             const float mb = mn != -INFINITY ? mn * kLog2e : 0.f;
             uint32_t ph[32], pl[32];
-            float lsum = 0.f;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kTcTok; c += 2) {
-                const float p0 = fast_exp2(fmaf(sv[c], kLog2e, -mb));
-                const float p1 = fast_exp2(fmaf(sv[c + 1], kLog2e, -mb));
-                lsum += p0 + p1;
+                const float p0 = fast_exp2(fmaf(x[c], cf, -mb));
+                const float p1 = fast_exp2(fmaf(x[c + 1], cf, -mb));
+                ls[(c >> 1) & 3] += p0 + p1;
                 const uint32_t h = E::pack(p0, p1);
                 ph[c >> 1] = h;
                 pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
             }
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_run = fmaf(l_run, a, lsum);
             m_run = mn;
 
@@ -383,9 +429,9 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 // 0 * garbage cannot reach O.
                 const int vt = tokE - (tok0 + t * kTcTok);
                 if (vt < kTcTok) {
-                    const int s = t % stages;
+                    const int s = t % vst;
                     if (!__all_sync(0xffffffffu,
-                                    mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / stages) & 1u,
+                                    mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u,
                                                         abort_flag))) {
                         ok = false;
                         break;

@@ -6,7 +6,7 @@ Every test forces that kernel (pa_set_rows_kernel(2)) and compares the CUDA
 path, V2 (partials + merge) and V1, element by element with the fp64 oracle,
 with the tolerances of parity_util: row counts below, at and above one CTA's
 128 rows, every head_dim and block size, K/V tiles that end inside a block,
-partitions that begin inside a block, a ring of one to five stages, chunked
+partitions that begin inside a block, K and V rings of one to five stages, chunked
 prefill (a chunk of new tokens attending to a cached prefix and causally to
 itself), poisoned caches and bad block ids.
 """
@@ -72,12 +72,11 @@ def test_tc_head_dims_and_block_sizes(D, bs, dtype):
     check_mq(wl.make_inputs(w, device="cuda"), P)
 
 
-@pytest.mark.parametrize("stages", [1, 3, 5])
-def test_tc_ring_stages(cuda_lib, stages):
-    """The K/V ring wraps many times (V1 walks 1000+ tokens); a request for
-    one stage runs with two."""
-    cuda_lib.pa_set_launch_config(0, stages)
-    w = mq("tc_stages", 8, 4, (700, 1100, 64), P=256, seed=8300 + stages)
+@pytest.mark.parametrize("k_stages,v_stages", [(1, 1), (3, 1), (1, 3), (2, 2), (5, 4)])
+def test_tc_ring_stages(cuda_lib, k_stages, v_stages):
+    """The K and V rings wrap many times (V1 walks 1000+ tokens)."""
+    cuda_lib.pa_set_launch_config(v_stages, k_stages)
+    w = mq("tc_stages", 8, 4, (700, 1100, 64), P=256, seed=8300 + 8 * k_stages + v_stages)
     check_mq(wl.make_inputs(w, device="cuda"), 256)
 
 
