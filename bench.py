@@ -35,10 +35,20 @@ import workloads as wl  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "paged-decode attention effective KV-read GB/s (% of HBM peak); µs per call"
 DEFAULT_CONFIG = "batch_decode"
-KERNEL_SOURCES = ["paged_kv_decode_v2_gb300/csrc/pa_attn.cuh",
-                  "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"]
+# Sources of each kernel family, hashed to void a recorded ncu traffic figure
+# once the kernel changes.
+KERNEL_SOURCES = {
+    "pa_attn": ["paged_kv_decode_v2_gb300/csrc/pa_attn.cuh",
+                "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
+    "pa_tc": ["paged_kv_decode_v2_gb300/csrc/pa_tc.cuh",
+              "paged_kv_decode_v2_gb300/csrc/pa_tcgen05.cuh",
+              "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
+}
+# From this many query rows per KV head the library runs the tcgen05 kernel.
+TC_MIN_ROWS = 64
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -78,6 +88,17 @@ def hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bf16_peak():
+    """Dense bf16 tensor TFLOP/s: the measured burst figure (a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 class ClockSampler:
@@ -143,9 +164,9 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(family: str = "pa_attn") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -159,7 +180,7 @@ def recorded_traffic(workload: str, kernel: str):
             rec = json.load(f)[f"{kernel}/{workload}"]
     except Exception:
         return None
-    if rec.get("source_hash") != kernel_source_hash():
+    if rec.get("source_hash") != kernel_source_hash(kernel.split("_v")[0]):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -190,24 +211,37 @@ class Decoder:
         self.cap = base.block_tables.shape[1] * w.block_size
         self.max_seq_len = base.max_seq_len
         self.np = pa.num_partitions(self.max_seq_len, w.partition_size)
-        self.tmp, self.es, self.ml = pa.alloc_workspace(S, H, D, max(1, self.np), device=device,
-                                                        q_len=w.q_len)
         self.out = torch.empty_like(base.query)
         if w.q_len > 1:
-            self.variant = 2  # several new tokens: the two-pass multi-query entry point
+            # several new tokens: the multi-query dispatch entry point
+            self.variant = pa.pa_decode_mq_choose(S, w.q_len, w.num_heads, w.num_kv_heads,
+                                                  self.max_seq_len, w.partition_size)
         else:
             self.variant = pa.pa_decode_choose(S, w.num_kv_heads, self.max_seq_len,
                                                w.partition_size)
         self.launches_per_step = 2 if self.variant == 2 else 1
+        # V1 with several new tokens never touches the intermediates: one slot suffices.
+        np_alloc = 1 if (w.q_len > 1 and self.variant == 1) else max(1, self.np)
+        self.tmp, self.es, self.ml = pa.alloc_workspace(S, H, D, np_alloc, device=device,
+                                                        q_len=w.q_len)
+        # Algorithmic FLOPs of a call: 4 * head_dim per (query row, head, visible
+        # key) -- Q.K and P.V, 2 * head_dim each; new token i of a sequence of
+        # L tokens sees L - q_len + i + 1 keys.
+        vis = 0
+        for L in base.seq_lens.tolist():
+            for i in range(w.q_len):
+                vis += max(0, min(L - w.q_len + i + 1, L))
+        self.flops = 4 * w.head_dim * w.num_heads * vis
+        self.family = "pa_tc" if w.q_len * w.group_size >= TC_MIN_ROWS else "pa_attn"
 
     def call(self, i: int):
         """One decode call on copy i % R through the public dispatch entry point."""
         pa, w, inp = self.pa, self.w, self.inp
         kc, vc = self.caches[i % self.copies]
         if w.q_len > 1:
-            pa.pa_decode_v2_mq(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
-                               w.partition_size, self.out, self.tmp, self.es, self.ml,
-                               max_seq_len_hint=self.max_seq_len)
+            pa.pa_decode_mq(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
+                            w.partition_size, self.out, self.tmp, self.es, self.ml,
+                            max_seq_len_hint=self.max_seq_len)
             return
         pa.pa_decode(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, w.partition_size,
                      self.out, self.tmp, self.es, self.ml, max_seq_len_hint=self.max_seq_len)
@@ -257,8 +291,8 @@ class Decoder:
         q, bt, sl = self.e2e_inputs
         kc, vc = self.caches[i % self.copies]
         if w.q_len > 1:
-            pa.pa_decode_v2_mq(q, kc, vc, bt, sl, w.scale, w.partition_size, self.out, self.tmp,
-                               self.es, self.ml, max_seq_len_hint=self.max_seq_len)
+            pa.pa_decode_mq(q, kc, vc, bt, sl, w.scale, w.partition_size, self.out, self.tmp,
+                            self.es, self.ml, max_seq_len_hint=self.max_seq_len)
         else:
             pa.pa_decode(q, kc, vc, bt, sl, w.scale, w.partition_size, self.out, self.tmp, self.es,
                          self.ml, max_seq_len_hint=self.max_seq_len)
@@ -339,9 +373,13 @@ def time_gpu(args, w: wl.Workload):
 
     gbs = world * dec.kv_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    kernel = "pa_attn_v2_phase1" if dec.variant == 2 else "pa_attn_v1"
+    tpeak, tpeak_kind = bf16_peak()
+    kernel = dec.family + ("_v2_phase1" if dec.variant == 2 else "_v1")
     k1_gbs = dec.kv_bytes / (k1_ms * 1e-3) / 1e9
+    k1_tflops = dec.flops / (k1_ms * 1e-3) / 1e12
     traffic = recorded_traffic(w.name, kernel)
+    # The bound: whichever of HBM bytes and tensor FLOPs takes longer at its peak.
+    tensor_bound = dec.flops / (tpeak * 1e12) > dec.kv_bytes / (peak * 1e9)
     result = {
         "metric": METRIC,
         "value": round(gbs, 2),
@@ -371,15 +409,22 @@ def time_gpu(args, w: wl.Workload):
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * dec.launches_per_step,
-        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2),
-                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(k1_gbs / peak, 4), "traffic": traffic,
+        "roofline": ({"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2),
+                      "peak": tpeak, "peak_kind": tpeak_kind + " dense bf16 (burst)",
+                      "unit": "TFLOP/s", "frac": round(k1_tflops / tpeak, 4)}
+                     if tensor_bound else
+                     {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2),
+                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                      "frac": round(k1_gbs / peak, 4)}) | {
+                     "traffic": traffic,
                      "algorithmic_bytes_per_launch": dec.kv_bytes,
+                     "algorithmic_flops_per_launch": dec.flops,
                      "kernel_us": round(k1_ms * 1e3, 3),
                      "timing": ("kernel 1 alone, CUDA events around it on its stream, "
                                 "averaged over K split calls right after the timed region")
                                if w.q_len == 1 else
-                               "whole call (both kernels), CUDA events, K calls after the timed region",
+                               "whole call (its one or two kernels), CUDA events, K calls after "
+                               "the timed region",
                      "merge_us": round(k2_ms * 1e3, 3) if dec.variant == 2 else None},
         "clocks": clocks,
     }
@@ -389,14 +434,22 @@ def time_gpu(args, w: wl.Workload):
 # ---------------------------------------------------------------- the oracle on the host
 
 def time_oracle(w: wl.Workload, budget_s: float = 12.0):
-    """The fp64 oracle as it stands, on all host cores, over a bounded sample of the workload."""
+    """The fp64 oracle as it stands, on all host cores, over a bounded sample of the workload.
+
+    The sample is a seeded random subset of the (query row, head) pairs; the
+    time of the whole workload is extrapolated by the keys the pairs see, and
+    the line's GB/s is the workload's K/V bytes over that time.
+    """
     import oracle
     inp = wl.make_inputs(w, device="cpu")
     prob = oracle.Problem.from_arrays(wl.to_oracle_arrays(inp))
     cores = os.cpu_count() or 1
-    S, H = w.num_seqs, w.num_heads
-    order = list(range(S * H))
-    # grow the sample of (seq, head) pairs until one pass takes a noticeable time
+    S, Q, H = w.num_seqs, w.q_len, w.num_heads
+    lens = inp.seq_lens.tolist()
+    keys = [max(0, min(lens[r // Q] - Q + r % Q + 1, lens[r // Q])) for r in range(S * Q)]
+    total_keys = sum(keys) * H
+    order = torch.randperm(S * Q * H, generator=torch.Generator().manual_seed(w.seed)).tolist()
+    # grow the sample of (row, head) pairs until one pass takes a noticeable time
     n = max(1, min(len(order), 64))
     while True:
         pairs = [(i // H, i % H) for i in order[:n]]
@@ -411,12 +464,13 @@ def time_oracle(w: wl.Workload, budget_s: float = 12.0):
     for _ in range(reps):
         oracle.decode(prob, pairs=pairs, num_threads=cores)
     dt = (time.perf_counter() - t) / reps
-    lens = inp.seq_lens.tolist()
-    sample_bytes = sum(lens[b] * w.head_dim * 2 * 2 for b, h in pairs) // w.group_size
-    gbs = sample_bytes / dt / 1e9
-    desc = (f"{len(pairs)} of {S * H} (seq, head) pairs of {w.name}"
-            f"{' (all)' if len(pairs) == S * H else ''}, {reps} timed passes of {dt:.2f} s")
-    return gbs, cores, desc, dt * (S * H) / len(pairs)
+    sample_keys = max(1, sum(keys[r] for r, _ in pairs))
+    full_s = dt * total_keys / sample_keys
+    gbs = inp.kv_bytes / full_s / 1e9
+    desc = (f"{len(pairs)} of {S * Q * H} (query row, head) pairs of {w.name}"
+            f"{' (all)' if len(pairs) == S * Q * H else ''}, {reps} timed passes of {dt:.2f} s, "
+            f"extrapolated by visible keys")
+    return gbs, cores, desc, full_s
 
 
 def main():

@@ -209,6 +209,32 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
                            int32_t *status, pa_stream_t stream);
 
 /*
+ * Which variant pa_decode_mq runs for q_len new tokens per sequence on the
+ * current device: returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.
+ * Host only.  V1 when one partition covers max_seq_len, or when the V1 grid
+ * (num_seqs * num_kv_heads CTAs for every CTA that splits a KV head's
+ * q_len * G query rows) gives every SM at least one CTA and a KV head has
+ * at least 16 query rows; otherwise V2.  There is no counterpart in the
+ * method's description, which dispatches single-token decode only.
+ */
+PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
+                               int max_seq_len, int partition_size);
+
+/*
+ * pa_decode_v2_mq or pa_decode_v1_mq, as pa_decode_mq_choose picks (the
+ * capacity max_seq_len_hint if > 0, else max_blocks_per_seq * block_size, is
+ * its max_seq_len).  The V2 intermediates must be valid whenever V2 can be
+ * chosen.
+ */
+PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int q_len, int num_heads, int num_kv_heads, int head_dim,
+                        int num_blocks, int block_size, int max_blocks_per_seq,
+                        int max_seq_len_hint, float scale, int partition_size, int dtype,
+                        void *out, float *tmp_output, float *exp_sums, float *max_logits,
+                        int max_num_partitions, int32_t *status, pa_stream_t stream);
+
+/*
  * Single-pass decode: one CTA per (sequence, KV head) walks all blocks with
  * a running {m, l, o} and writes `out` directly.  No intermediates.
  */

@@ -70,6 +70,10 @@ def load() -> ctypes.CDLL:
     lib.pa_decode.restype = I
     lib.pa_decode_choose.argtypes = [I, I, I, I]
     lib.pa_decode_choose.restype = I
+    lib.pa_decode_mq.argtypes = attn_mq + [I, I, P, P, P, P, I, P, P]
+    lib.pa_decode_mq.restype = I
+    lib.pa_decode_mq_choose.argtypes = [I, I, I, I, I, I]
+    lib.pa_decode_mq_choose.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_launch_config.argtypes = [I, I]
@@ -206,6 +210,29 @@ def pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, scale
     rc = lib.pa_decode_v1_mq(*args, _DTYPE[query.dtype], _ptr(out), _ptr(status), _stream(stream))
     _check("pa_decode_v1_mq", rc)
     return out
+
+
+def pa_decode_mq(query, key_cache, value_cache, block_tables, seq_lens, scale, partition_size,
+                 out, tmp_output, exp_sums, max_logits, max_seq_len_hint=0, status=None,
+                 stream=None):
+    """Several new tokens per sequence, V1 or V2 as pa_decode_mq_choose picks."""
+    lib = load()
+    args = _shape_args_mq(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint,
+                          scale)
+    rc = lib.pa_decode_mq(*args, int(partition_size), _DTYPE[query.dtype], _ptr(out),
+                          _ptr(tmp_output), _ptr(exp_sums), _ptr(max_logits),
+                          tmp_output.shape[-2], _ptr(status), _stream(stream))
+    _check("pa_decode_mq", rc)
+    return out
+
+
+def pa_decode_mq_choose(num_seqs: int, q_len: int, num_heads: int, num_kv_heads: int,
+                        max_seq_len: int, partition_size: int) -> int:
+    r = load().pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, max_seq_len,
+                                   partition_size)
+    if r < 0:
+        raise PagedAttentionError("pa_decode_mq_choose", -r)
+    return r
 
 
 def pa_decode_v1(query, key_cache, value_cache, block_tables, seq_lens, scale, out,

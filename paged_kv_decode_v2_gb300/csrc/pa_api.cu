@@ -343,6 +343,21 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+// Whether the query rows of a KV head (q_len * G of them) go to the tcgen05 kernel.
+bool use_tc(int cols)
+{
+    const int mode = g_rows_kernel.load(std::memory_order_relaxed);
+    return mode == 2 || (mode == 0 && cols >= kTcMinRows);
+}
+
+// CTAs that split the query rows of one KV head and range.
+int row_ctas(int cols)
+{
+    if (use_tc(cols))
+        return (cols + kTcRows - 1) / kTcRows;
+    return cols <= 8 ? 1 : (cols + kMaxGroup - 1) / kMaxGroup;
+}
+
 // Builds the attention launch (V2 phase 1 or V1) after validation.
 int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const void *value_cache,
                const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int q_len,
@@ -371,8 +386,7 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.group = num_heads / num_kv_heads;
     p.q_len = q_len;
     p.cols = p.group * q_len;
-    const int mode = g_rows_kernel.load(std::memory_order_relaxed);
-    L.tc = mode == 2 || (mode == 0 && p.cols >= kTcMinRows);
+    L.tc = use_tc(p.cols);
     if (L.tc) {
         // 128 rows per CTA; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
@@ -508,6 +522,24 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
     return pa_v2_num_partitions(max_seq_len, partition_size) <= 1 ? 1 : 2;
 }
 
+// Several new tokens per sequence: V1 when one partition covers the
+// sequences, or when its grid (num_seqs * num_kv_heads CTAs per row split)
+// already gives every SM a CTA and a KV head has at least 16 query rows, so
+// each CTA carries enough work; otherwise V2.  Measured on GB300, batch
+// decode (32 seqs up to 8192 tokens, 32 / 8 heads) checking q_len tokens:
+// q_len 2: V2 92 vs V1 100 us; 4: V1 113 vs 123; 8: V1 157 vs 223; 32: V1
+// 230 vs 289; 100K-token sequence, q_len 16: V2 103 vs V1 2229 us; chunked
+// prefill (2 x 2048 new tokens after 30K): V1 3579 vs V2 6129 us.
+int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int max_seq_len,
+                      int partition_size, int sms)
+{
+    if (pa_v2_num_partitions(max_seq_len, partition_size) <= 1)
+        return 1;
+    const int cols = q_len * group;
+    const long long ctas = (long long)num_seqs * num_kv_heads * row_ctas(cols);
+    return (cols >= 16 && ctas >= sms) ? 1 : 2;
+}
+
 } // namespace
 
 extern "C" {
@@ -639,6 +671,56 @@ PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int
     if (sms <= 0)
         return -PA_ERR_CUDA;
     return choose_variant(num_seqs, num_kv_heads, max_seq_len, partition_size, sms);
+}
+
+PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
+                               int max_seq_len, int partition_size)
+{
+    if (num_seqs <= 0 || q_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || max_seq_len < 0 || partition_size <= 0)
+        return -PA_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(&dev))
+        return -PA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return -PA_ERR_CUDA;
+    return choose_variant_mq(num_seqs, q_len, num_heads / num_kv_heads, num_kv_heads, max_seq_len,
+                             partition_size, sms);
+}
+
+PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
+                        const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                        int q_len, int num_heads, int num_kv_heads, int head_dim,
+                        int num_blocks, int block_size, int max_blocks_per_seq,
+                        int max_seq_len_hint, float scale, int partition_size, int dtype,
+                        void *out, float *tmp_output, float *exp_sums, float *max_logits,
+                        int max_num_partitions, int32_t *status, pa_stream_t stream)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    rc = check_q_len(num_seqs, q_len);
+    if (rc)
+        return rc;
+    if (partition_size <= 0)
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    const int which =
+        pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, cap, partition_size);
+    if (which < 0)
+        return -which;
+    if (which == 1)
+        return pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                               q_len, num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                               max_blocks_per_seq, max_seq_len_hint, scale, dtype, out, status,
+                               stream);
+    return pa_decode_v2_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                           num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                           max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype, out,
+                           tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
 }
 
 PA_API int pa_decode(const void *query, const void *key_cache, const void *value_cache,

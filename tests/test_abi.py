@@ -23,7 +23,8 @@ def test_header_declares_the_entry_points():
     for n in ("pa_decode_v2", "pa_decode_v1", "pa_decode", "pa_decode_v2_phase1",
               "pa_decode_v2_phase2", "pa_v2_num_partitions", "pa_v2_workspace_bytes",
               "pa_status_string", "pa_decode_choose", "pa_selftest_wait_timeout",
-              "pa_set_launch_config", "pa_set_rows_kernel"):
+              "pa_set_launch_config", "pa_set_rows_kernel", "pa_decode_mq",
+              "pa_decode_mq_choose"):
         assert n in names
 
 
@@ -108,6 +109,18 @@ def test_launch_config_override_validation(cuda_lib):
     assert cuda_lib.load().pa_set_launch_config(9, 2) == 1
     assert cuda_lib.load().pa_set_launch_config(4, 9) == 1
     assert cuda_lib.load().pa_set_launch_config(0, 0) == 0
+
+
+def test_multi_query_dispatch_validation(cuda_lib):
+    lib = cuda_lib.load()
+    assert lib.pa_decode_mq_choose(0, 4, 32, 8, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 0, 32, 8, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 4, 30, 8, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 4, 32, 8, 1000, 0) == -1
+    args = [FAKE] * 5 + [1, 0, 8, 2, 128, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_mq(*args, 512, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
+    args = [FAKE] * 5 + [1, 4, 8, 2, 128, 128, 16, 63, 0, 0.088]
+    assert lib.pa_decode_mq(*args, 0, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
 
 
 def test_rows_kernel_override_validation(cuda_lib):

@@ -141,3 +141,26 @@ def test_tc_speculative_batch_full_size():
     """Batch decode (32 seqs up to 8192 tokens, 32/8 heads) checking 8 speculated tokens each."""
     w = wl.BATCH.with_(name="batch_spec8", q_len=8)
     check_mq(wl.make_inputs(w, device="cuda"), w.partition_size)
+
+
+def test_tc_spec_verify_16_full_size():
+    """Batch decode checking 16 speculated tokens (64 query rows per KV head), every element."""
+    w = wl.SPEC_VERIFY16
+    check_mq(wl.make_inputs(w, device="cuda"), w.partition_size)
+
+
+def test_tc_chunked_prefill_full_size_sampled():
+    """2 x (30,720-token prefix + 2048-token chunk): sampled query rows (first, last, tile and
+    chunk edges) of three heads, V1 and V2, against the oracle."""
+    w = wl.CHUNKED_PREFILL
+    inp = wl.make_inputs(w, device="cuda")
+    prob = oracle_problem(inp)
+    Q = w.q_len
+    rows = [0, 1, 63, 64, 1000, Q - 1, Q, Q + 517, 2 * Q - 1]
+    heads = [0, 7, 31]
+    pairs = [(r, h) for r in rows for h in heads]
+    ref = oracle.decode(prob, pairs=pairs)
+    for e in ("v1", "v2"):
+        out = run_mq(inp, w.partition_size, entry=e)[0]
+        g = torch.stack([out[r // Q, r % Q, h] for r, h in pairs])
+        check_out(g, ref, w.dtype, what=f"{w.name}/{e}")

@@ -82,7 +82,15 @@ STRESS = Workload("stress", 8, 64, 8, 128, 16, 1024, F16, "fixed", seq_len=13107
 # Batch decode checking 4 speculated tokens per sequence (several new tokens per call).
 BATCH_SPEC4 = BATCH.with_(name="batch_decode_spec4", q_len=4)
 
-ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS, BATCH_SPEC4)}
+# Batch decode checking 16 speculated tokens per sequence: 64 query rows per KV head.
+SPEC_VERIFY16 = BATCH.with_(name="spec_verify_16", q_len=16)
+# Chunked prefill: 2 sequences, each adding a 2048-token chunk (already written
+# to the cache) after a 30,720-token prefix; 32 query / 8 KV heads.
+CHUNKED_PREFILL = Workload("chunked_prefill", 2, 32, 8, 128, 16, 512, BF16, "fixed",
+                           seq_len=32768, q_len=2048, seed=20261207)
+
+ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS, BATCH_SPEC4,
+                           SPEC_VERIFY16, CHUNKED_PREFILL)}
 
 
 def draw_seq_lens(w: Workload) -> list:
