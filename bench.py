@@ -214,7 +214,7 @@ class Decoder:
         self.out = torch.empty_like(base.query)
         if w.q_len > 1:
             # several new tokens: the multi-query dispatch entry point
-            self.variant = pa.pa_decode_mq_choose(S, w.q_len, w.num_heads, w.num_kv_heads,
+            self.variant = pa.pa_decode_mq_choose(S, w.q_len, w.num_heads, w.num_kv_heads, D,
                                                   self.max_seq_len, w.partition_size)
         else:
             self.variant = pa.pa_decode_choose(S, w.num_kv_heads, self.max_seq_len,

@@ -218,7 +218,7 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
  * method's description, which dispatches single-token decode only.
  */
 PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
-                               int max_seq_len, int partition_size);
+                               int head_dim, int max_seq_len, int partition_size);
 
 /*
  * pa_decode_v2_mq or pa_decode_v1_mq, as pa_decode_mq_choose picks (the
@@ -275,9 +275,12 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
 /*
  * Kernel choice for the query rows of a KV head (rows = q_len * G),
  * process-wide: 0 (default) picks by row count -- up to 63 rows the
- * mma.sync kernel (16 rows per CTA), from 64 rows the tcgen05 kernel (128
- * rows per CTA, S and O accumulated in tensor memory); 1 always the mma.sync
- * kernel; 2 always the tcgen05 kernel.  Either kernel computes the same
+ * mma.sync kernel (16 rows per CTA), from 64 rows a tcgen05 kernel (128-row
+ * query tiles, S and O accumulated in tensor memory; two tiles sharing each
+ * K/V tile per CTA when a KV head has more than 128 rows and head_dim <=
+ * 128); 1 always the mma.sync kernel; 2 always a tcgen05 kernel; 3 always
+ * the one-tile tcgen05 kernel; 4 always the two-tile one (one tile for
+ * head_dim 256).  Either kernel computes the same
  * result within the stated tolerances; the choice changes only speed.  The
  * tcgen05 kernel takes its K ring stages from pa_set_launch_config's
  * stages_per_warp and its V ring stages from warps_per_cta when those are

@@ -72,7 +72,7 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_choose.restype = I
     lib.pa_decode_mq.argtypes = attn_mq + [I, I, P, P, P, P, I, P, P]
     lib.pa_decode_mq.restype = I
-    lib.pa_decode_mq_choose.argtypes = [I, I, I, I, I, I]
+    lib.pa_decode_mq_choose.argtypes = [I, I, I, I, I, I, I]
     lib.pa_decode_mq_choose.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -227,9 +227,9 @@ def pa_decode_mq(query, key_cache, value_cache, block_tables, seq_lens, scale, p
 
 
 def pa_decode_mq_choose(num_seqs: int, q_len: int, num_heads: int, num_kv_heads: int,
-                        max_seq_len: int, partition_size: int) -> int:
-    r = load().pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, max_seq_len,
-                                   partition_size)
+                        head_dim: int, max_seq_len: int, partition_size: int) -> int:
+    r = load().pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, head_dim,
+                                   max_seq_len, partition_size)
     if r < 0:
         raise PagedAttentionError("pa_decode_mq_choose", -r)
     return r
@@ -267,7 +267,8 @@ def pa_set_launch_config(warps_per_cta: int = 0, stages_per_warp: int = 0) -> No
 
 
 def pa_set_rows_kernel(mode: int = 0) -> None:
-    """0: pick the attention kernel by query rows per KV head; 1: always mma.sync; 2: always tcgen05."""
+    """0: by query rows per KV head; 1: always mma.sync; 2: always tcgen05; 3: tcgen05, one
+    query tile per CTA; 4: tcgen05, two query tiles per CTA."""
     _check("pa_set_rows_kernel", load().pa_set_rows_kernel(mode))
 
 

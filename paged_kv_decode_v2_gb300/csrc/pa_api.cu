@@ -20,7 +20,8 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_tune_warps{0};
 std::atomic<int> g_tune_stages{0};
 // Kernel for the query rows of a KV head: 0 = by row count, 1 = always the
-// mma.sync kernel, 2 = always the tcgen05 kernel.
+// mma.sync kernel, 2 = always a tcgen05 kernel (query tiles by row count),
+// 3 = the one-tile tcgen05 kernel, 4 = the two-tile one (head_dim <= 128).
 std::atomic<int> g_rows_kernel{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
@@ -275,32 +276,39 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
 }
 
 // Per-device dynamic shared memory limit of each tcgen05 kernel after the opt-in.
-constexpr int kTcSlots = 2 * 3 * 3 * 2;
+constexpr int kTcSlots = 2 * 3 * 3 * 2 * 2;
 std::atomic<int> g_tc_smem_limit[kMaxDevices][kTcSlots];
 
-int tc_slot(int dtype, int head_dim, int block_size, bool v1)
+int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles)
 {
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
     const int bi = block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
-    return (((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (v1 ? 1 : 0);
+    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (v1 ? 1 : 0)) * 2 + (tiles - 1);
 }
 
-// The tcgen05 kernel: as many K and V ring stages as keep two CTAs per SM
-// for head_dim <= 128 (one for 256 dims, whose TMEM takes the whole SM).
+// The tcgen05 kernels.  One query tile: as many K and V ring stages as keep
+// two CTAs per SM for head_dim <= 128 (one for 256 dims, whose TMEM takes
+// the whole SM).  Two query tiles (one CTA per SM, all 512 TMEM columns):
+// 2 + 2 stages of 128 tokens at head_dim 128, 4 + 4 at 64.
 // pa_set_launch_config's stages_per_warp overrides the K stages and its
 // warps_per_cta the V stages.
 int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
 {
-    const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1);
+    const int tiles = L.tc_tiles;
+    const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1, tiles);
     size_t limit = (size_t)g_tc_smem_limit[dev][slot].load(std::memory_order_acquire);
     if (limit == 0) {
         int optin = 0;
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return PA_ERR_CUDA;
-        if (tc_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.v1, optin, &limit) != cudaSuccess)
+        if (tc_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.v1, tiles, optin, &limit) !=
+            cudaSuccess)
             return PA_ERR_CUDA;
         g_tc_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
     }
+    auto bytes = [&](int ks, int vs) {
+        return tiles == 2 ? tc2_smem_bytes(L.head_dim, ks, vs) : tc_smem_bytes(L.head_dim, ks, vs);
+    };
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
     const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
     int ks = L.head_dim == 64 ? 4 : 2, vs = ks;
@@ -308,18 +316,18 @@ int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
         ks = tune_s;
     if (tune_w > 0)
         vs = tune_w;
-    while (tc_smem_bytes(L.head_dim, ks, vs) > limit && (ks > 1 || vs > 1)) {
+    while (bytes(ks, vs) > limit && (ks > 1 || vs > 1)) {
         if (ks >= vs)
             --ks;
         else
             --vs;
     }
-    if (tc_smem_bytes(L.head_dim, ks, vs) > limit)
+    if (bytes(ks, vs) > limit)
         return PA_ERR_UNSUPPORTED;
     L.p.stages = ks;
     L.p.v_stages = vs;
-    L.warps = kTcThreads / 32;
-    L.smem_bytes = tc_smem_bytes(L.head_dim, ks, vs);
+    L.warps = (tiles == 2 ? kTc2Threads : kTcThreads) / 32;
+    L.smem_bytes = bytes(ks, vs);
     return tc_ops(L.dtype, L.head_dim)->launch(L, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -343,18 +351,28 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-// Whether the query rows of a KV head (q_len * G of them) go to the tcgen05 kernel.
+// Whether the query rows of a KV head (q_len * G of them) go to a tcgen05 kernel.
 bool use_tc(int cols)
 {
     const int mode = g_rows_kernel.load(std::memory_order_relaxed);
-    return mode == 2 || (mode == 0 && cols >= kTcMinRows);
+    return mode >= 2 || (mode == 0 && cols >= kTcMinRows);
+}
+
+// 128-row query tiles per CTA of the tcgen05 kernel: two when a KV head has
+// more than 128 rows and two tiles' O and S fit the SM's 512 TMEM columns.
+int tc_tiles(int cols, int head_dim)
+{
+    const int mode = g_rows_kernel.load(std::memory_order_relaxed);
+    if (head_dim > 128 || mode == 3)
+        return 1;
+    return (mode == 4 || cols > kTcRows) ? 2 : 1;
 }
 
 // CTAs that split the query rows of one KV head and range.
-int row_ctas(int cols)
+int row_ctas(int cols, int head_dim)
 {
     if (use_tc(cols))
-        return (cols + kTcRows - 1) / kTcRows;
+        return (cols + kTcRows * tc_tiles(cols, head_dim) - 1) / (kTcRows * tc_tiles(cols, head_dim));
     return cols <= 8 ? 1 : (cols + kMaxGroup - 1) / kMaxGroup;
 }
 
@@ -388,9 +406,10 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.cols = p.group * q_len;
     L.tc = use_tc(p.cols);
     if (L.tc) {
-        // 128 rows per CTA; the CTAs of one range split the rows.
+        // 128 rows per query tile; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
-        p.col_groups = (p.cols + kTcRows - 1) / kTcRows;
+        L.tc_tiles = tc_tiles(p.cols, head_dim);
+        p.col_groups = row_ctas(p.cols, head_dim);
     } else {
         // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
         L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
@@ -530,13 +549,13 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 // q_len 2: V2 92 vs V1 100 us; 4: V1 113 vs 123; 8: V1 157 vs 223; 32: V1
 // 230 vs 289; 100K-token sequence, q_len 16: V2 103 vs V1 2229 us; chunked
 // prefill (2 x 2048 new tokens after 30K): V1 3579 vs V2 6129 us.
-int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int max_seq_len,
-                      int partition_size, int sms)
+int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int head_dim,
+                      int max_seq_len, int partition_size, int sms)
 {
     if (pa_v2_num_partitions(max_seq_len, partition_size) <= 1)
         return 1;
     const int cols = q_len * group;
-    const long long ctas = (long long)num_seqs * num_kv_heads * row_ctas(cols);
+    const long long ctas = (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim);
     return (cols >= 16 && ctas >= sms) ? 1 : 2;
 }
 
@@ -674,10 +693,10 @@ PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int
 }
 
 PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
-                               int max_seq_len, int partition_size)
+                               int head_dim, int max_seq_len, int partition_size)
 {
     if (num_seqs <= 0 || q_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 ||
-        num_heads % num_kv_heads != 0 || max_seq_len < 0 || partition_size <= 0)
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || max_seq_len < 0 || partition_size <= 0)
         return -PA_ERR_INVALID_ARG;
     int dev;
     if (current_device(&dev))
@@ -685,8 +704,8 @@ PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_k
     const int sms = sm_count(dev);
     if (sms <= 0)
         return -PA_ERR_CUDA;
-    return choose_variant_mq(num_seqs, q_len, num_heads / num_kv_heads, num_kv_heads, max_seq_len,
-                             partition_size, sms);
+    return choose_variant_mq(num_seqs, q_len, num_heads / num_kv_heads, num_kv_heads, head_dim,
+                             max_seq_len, partition_size, sms);
 }
 
 PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
@@ -709,7 +728,7 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
         return PA_ERR_INVALID_ARG;
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     const int which =
-        pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, cap, partition_size);
+        pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, head_dim, cap, partition_size);
     if (which < 0)
         return -which;
     if (which == 1)
@@ -777,7 +796,7 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp)
 
 PA_API int pa_set_rows_kernel(int mode)
 {
-    if (mode < 0 || mode > 2)
+    if (mode < 0 || mode > 4)
         return PA_ERR_INVALID_ARG;
     g_rows_kernel.store(mode, std::memory_order_relaxed);
     return PA_OK;

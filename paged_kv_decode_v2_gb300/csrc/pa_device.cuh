@@ -90,6 +90,22 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+// try_wait that lets the hardware suspend the thread (up to 100 us) until the
+// phase completes, instead of returning at once: a waiting warp then takes
+// no issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(100000u)
+        : "memory");
+    return ok != 0;
+}
+
 // mbar_wait_bounded that also gives up as soon as *abort is non-zero (another
 // role of the CTA gave up first), so one stuck copy ends every wait quickly.
 __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parity,
@@ -99,9 +115,9 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint32_t bar, uint32_t parit
         return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1; it < (1u << 26); ++it) {
-        if (mbar_try_wait(bar, parity))
+        if (mbar_try_wait_suspend(bar, parity))
             return true;
-        if ((it & 63u) == 0 && (*abort || global_ns() - t0 > kWaitLimitNs))
+        if (*abort || global_ns() - t0 > kWaitLimitNs)
             return false;
     }
     return false;

@@ -19,6 +19,8 @@ constexpr int kMergeThreads = 128;   // phase-2 CTA size
 constexpr int kTcRows = 128;         // tcgen05 kernel: query rows per CTA (the MMA's M)
 constexpr int kTcTok = 64;           // tcgen05 kernel: tokens per K/V tile
 constexpr int kTcThreads = 192;      // tcgen05 kernel: 4 row warps, MMA warp, TMA warp
+constexpr int kTc2Tok = 128;         // two-tile tcgen05 kernel: tokens per K/V tile
+constexpr int kTc2Threads = 320;     // two-tile tcgen05 kernel: 8 row warps, MMA warp, TMA warp
 
 // Arguments of the attention kernel (phase 1 of V2, or V1).
 struct AttnParams {
@@ -54,7 +56,8 @@ struct AttnLaunch {
     int block_size;              // 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
-    bool tc;                     // the tcgen05 kernel (128 query rows per CTA)
+    bool tc;                     // a tcgen05 kernel
+    int tc_tiles;                // its 128-row query tiles per CTA (1 or 2)
     int cta_cols;                // query rows one CTA serves (<= 16): picks the n-tile count
     dim3 grid;
     int warps;
@@ -121,9 +124,17 @@ inline size_t tc_smem_bytes(int head_dim, int k_stages, int v_stages)
            (size_t)(k_stages + v_stages) * kTcTok * head_dim * 2;
 }
 
+// Dynamic shared memory of the two-tile tcgen05 kernel: two Q tiles, k_stages
+// K tiles and v_stages V tiles of 128 tokens, and the 1 KB alignment slack.
+inline size_t tc2_smem_bytes(int head_dim, int k_stages, int v_stages)
+{
+    return 1024 + (size_t)2 * kTcRows * head_dim * 2 +
+           (size_t)(k_stages + v_stages) * kTc2Tok * head_dim * 2;
+}
+
 // Entry points of the tcgen05 attention kernels for one (storage type, head_dim).
 struct TcOps {
-    cudaError_t (*prepare)(int block_size, bool v1, int optin_bytes, size_t *limit);
+    cudaError_t (*prepare)(int block_size, bool v1, int tiles, int optin_bytes, size_t *limit);
     cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
 };
 const TcOps *tc_ops_f16_d64();

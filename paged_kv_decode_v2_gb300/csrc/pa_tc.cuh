@@ -30,6 +30,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_tc2.cuh"
 #include "pa_tcgen05.cuh"
 
 namespace pa {
@@ -349,8 +350,10 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             }
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(lane_base + C::kSCol, sr[0]);
-            tmem_ld32(lane_base + C::kSCol + 32, sr[1]);
+            tmem_ld32_async(lane_base + C::kSCol, sr[0]);
+            tmem_ld32_async(lane_base + C::kSCol + 32, sr[1]);
+            tmem_ld_wait(sr[0]);
+            tmem_ld_wait(sr[1]);
             tc_fence_before();
             mbar_arrive(b_s_free);
 
@@ -409,19 +412,25 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
-                    for (int cc = 0; cc < D; cc += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(lane_base + cc, o);
+                    for (int cc = 0; cc < D; cc += 64) {
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32_async(lane_base + cc, o0);
+                        tmem_ld32_async(lane_base + cc + 32, o1);
+                        tmem_ld_wait(o0);
+                        tmem_ld_wait(o1);
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * a);
-                        tmem_st32(lane_base + cc, o);
+                        for (int k = 0; k < 32; ++k) {
+                            o0[k] = __float_as_uint(__uint_as_float(o0[k]) * a);
+                            o1[k] = __float_as_uint(__uint_as_float(o1[k]) * a);
+                        }
+                        tmem_st32x2(lane_base + cc, o0, lane_base + cc + 32, o1);
                     }
                 }
             }
-            tmem_st32(lane_base + C::kPCol, ph);
             if (kBf16)
-                tmem_st32(lane_base + C::kPCol + 32, pl);
+                tmem_st32x2(lane_base + C::kPCol, ph, lane_base + C::kPCol + 32, pl);
+            else
+                tmem_st32(lane_base + C::kPCol, ph);
 
             if (t == ntiles - 1) {
                 // Tile rows past the range (unloaded blocks, slots past the
@@ -505,24 +514,33 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     }
 }
 
+// Kernel dispatch on block size, V1/V2 and query tiles per CTA (two only for head_dim <= 128).
 template <typename T, int D>
-static const void *tc_kernel_ptr(int block_size, bool v1)
+static const void *tc_kernel_ptr(int block_size, bool v1, int tiles)
 {
-#define PA_PICK(BS)                                                                               \
+#define PA_PICK(K, BS)                                                                            \
     if (block_size == BS)                                                                         \
-        return v1 ? reinterpret_cast<const void *>(&tc_attn_kernel<T, D, BS, true>)               \
-                  : reinterpret_cast<const void *>(&tc_attn_kernel<T, D, BS, false>);
-    PA_PICK(16)
-    PA_PICK(32)
-    PA_PICK(64)
+        return v1 ? reinterpret_cast<const void *>(&K<T, D, BS, true>)                            \
+                  : reinterpret_cast<const void *>(&K<T, D, BS, false>);
+    if (tiles == 2) {
+        if constexpr (D <= 128) {
+            PA_PICK(tc2_attn_kernel, 16)
+            PA_PICK(tc2_attn_kernel, 32)
+            PA_PICK(tc2_attn_kernel, 64)
+        }
+        return nullptr;
+    }
+    PA_PICK(tc_attn_kernel, 16)
+    PA_PICK(tc_attn_kernel, 32)
+    PA_PICK(tc_attn_kernel, 64)
 #undef PA_PICK
     return nullptr;
 }
 
 template <typename T, int D>
-static cudaError_t tc_prepare(int block_size, bool v1, int optin_bytes, size_t *limit)
+static cudaError_t tc_prepare(int block_size, bool v1, int tiles, int optin_bytes, size_t *limit)
 {
-    const void *fn = tc_kernel_ptr<T, D>(block_size, v1);
+    const void *fn = tc_kernel_ptr<T, D>(block_size, v1, tiles);
     if (!fn)
         return cudaErrorInvalidValue;
     cudaFuncAttributes fa;
@@ -538,14 +556,14 @@ static cudaError_t tc_prepare(int block_size, bool v1, int optin_bytes, size_t *
 template <typename T, int D>
 static cudaError_t tc_launch(const AttnLaunch &L, cudaStream_t stream)
 {
-    const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1);
+    const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1, L.tc_tiles);
     if (!fn)
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
                     const_cast<AttnParams *>(&L.p)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
-    cfg.blockDim = dim3(kTcThreads);
+    cfg.blockDim = dim3(L.tc_tiles == 2 ? kTc2Threads : kTcThreads);
     cfg.dynamicSmemBytes = L.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -113,10 +113,11 @@ def test_launch_config_override_validation(cuda_lib):
 
 def test_multi_query_dispatch_validation(cuda_lib):
     lib = cuda_lib.load()
-    assert lib.pa_decode_mq_choose(0, 4, 32, 8, 1000, 512) == -1
-    assert lib.pa_decode_mq_choose(4, 0, 32, 8, 1000, 512) == -1
-    assert lib.pa_decode_mq_choose(4, 4, 30, 8, 1000, 512) == -1
-    assert lib.pa_decode_mq_choose(4, 4, 32, 8, 1000, 0) == -1
+    assert lib.pa_decode_mq_choose(0, 4, 32, 8, 128, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 0, 32, 8, 128, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 4, 30, 8, 128, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 4, 32, 8, 0, 1000, 512) == -1
+    assert lib.pa_decode_mq_choose(4, 4, 32, 8, 128, 1000, 0) == -1
     args = [FAKE] * 5 + [1, 0, 8, 2, 128, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_mq(*args, 512, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
     args = [FAKE] * 5 + [1, 4, 8, 2, 128, 128, 16, 63, 0, 0.088]
@@ -126,7 +127,8 @@ def test_multi_query_dispatch_validation(cuda_lib):
 def test_rows_kernel_override_validation(cuda_lib):
     lib = cuda_lib.load()
     assert lib.pa_set_rows_kernel(-1) == 1
-    assert lib.pa_set_rows_kernel(3) == 1
+    assert lib.pa_set_rows_kernel(5) == 1
+    assert lib.pa_set_rows_kernel(4) == 0
     assert lib.pa_set_rows_kernel(2) == 0
     assert lib.pa_set_rows_kernel(0) == 0
 

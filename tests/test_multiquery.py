@@ -57,15 +57,15 @@ def test_mq_dispatch_rule_and_entry(cuda_lib):
     """pa_decode_mq runs the variant pa_decode_mq_choose names (bitwise the same output)."""
     import paged_kv_decode_v2_gb300 as pa
     # batch decode shapes (32 seqs, 32 / 8 heads, up to 8192 tokens, P = 512)
-    assert pa.pa_decode_mq_choose(32, 2, 32, 8, 8192, 512) == 2   # 8 rows per KV head
-    assert pa.pa_decode_mq_choose(32, 4, 32, 8, 8192, 512) == 1   # 16 rows, 256 CTAs
-    assert pa.pa_decode_mq_choose(32, 32, 32, 8, 8192, 512) == 1
-    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 100000, 512) == 2  # one long sequence
-    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 512, 512) == 1     # one partition
+    assert pa.pa_decode_mq_choose(32, 2, 32, 8, 128, 8192, 512) == 2   # 8 rows per KV head
+    assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 8192, 512) == 1   # 16 rows, 256 CTAs
+    assert pa.pa_decode_mq_choose(32, 32, 32, 8, 128, 8192, 512) == 1
+    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 100000, 512) == 2  # one long sequence
+    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 512, 512) == 1     # one partition
     w = mq("mq_dispatch", 4, 4, (3, 100, 700, 1500), P=256, seed=79)
     inp = wl.make_inputs(w, device="cuda")
     S, Q, H, D = inp.query.shape
-    want = pa.pa_decode_mq_choose(S, Q, H, w.num_kv_heads, inp.block_tables.shape[1] * w.block_size, 256)
+    want = pa.pa_decode_mq_choose(S, Q, H, w.num_kv_heads, D, inp.block_tables.shape[1] * w.block_size, 256)
     ref = run_mq(inp, 256, entry="v1" if want == 1 else "v2")[0]
     tmp, es, ml = pa.alloc_workspace(S, H, D, pa.num_partitions(inp.block_tables.shape[1] * w.block_size, 256), q_len=Q)
     out = torch.full_like(inp.query, float("nan"))

@@ -2,8 +2,9 @@
 the GQA group) per CTA, S = Q K^T and O += P V on the fifth-generation
 tensor cores with S, P and O in tensor memory.
 
-Every test forces that kernel (pa_set_rows_kernel(2)) and compares the CUDA
-path, V2 (partials + merge) and V1, element by element with the fp64 oracle,
+Every test forces each of the two tcgen05 kernels in turn (one or two 128-row
+query tiles per CTA; pa_set_rows_kernel 3 and 4) and compares the CUDA path,
+V2 (partials + merge) and V1, element by element with the fp64 oracle,
 with the tolerances of parity_util: row counts below, at and above one CTA's
 128 rows, every head_dim and block size, K/V tiles that end inside a block,
 partitions that begin inside a block, K and V rings of one to five stages, chunked
@@ -21,12 +22,15 @@ from parity_util import (check_mq, check_out, check_partitions, mq, oracle_probl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True)
-def _force_tc(cuda_lib):
+@pytest.fixture(autouse=True, params=[3, 4], ids=["one_tile", "two_tiles"])
+def _force_tc(request, cuda_lib):
+    """Each test runs with the one-tile kernel (128 query rows per CTA) and with
+    the two-tile kernel (two 128-row tiles sharing each 128-token K/V tile;
+    head_dim 256 stays on one tile)."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     cuda_lib.pa_set_launch_config(0, 0)
-    cuda_lib.pa_set_rows_kernel(2)
+    cuda_lib.pa_set_rows_kernel(request.param)
     yield
     cuda_lib.pa_set_rows_kernel(0)
     cuda_lib.pa_set_launch_config(0, 0)
