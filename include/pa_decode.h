@@ -48,7 +48,7 @@
  *   Partition slots p >= ceil(seq_lens[b]/partition_size) are left untouched.
  *   A sequence with seq_len 0 gets a zero output row.
  *
- * Supported shapes: head_dim 64, 128 or 256; block_size 16, 32 or 64;
+ * Supported shapes: head_dim 64, 128 or 256; block_size 8, 16, 32 or 64;
  * partition_size any positive value (a partition may begin or end inside a
  * block; a block that straddles two partitions is read by both); G = num_heads /
  * num_kv_heads an integer in [1, 64]; q_len in [1, 4096] with num_seqs *

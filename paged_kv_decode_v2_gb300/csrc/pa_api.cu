@@ -84,7 +84,7 @@ int check_shape(const void *query, const void *key_cache, const void *value_cach
         return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256)
         return PA_ERR_UNSUPPORTED;
-    if (block_size != 16 && block_size != 32 && block_size != 64)
+    if (block_size != 8 && block_size != 16 && block_size != 32 && block_size != 64)
         return PA_ERR_UNSUPPORTED;
     if (num_heads / num_kv_heads > kMaxGQA)
         return PA_ERR_UNSUPPORTED;
@@ -169,13 +169,13 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_bloc
 }
 
 // Index of a kernel instantiation: storage type x head_dim x block size x n-tiles x V1/V2.
-constexpr int kKernelSlots = 2 * 3 * 3 * 2 * 2;
+constexpr int kKernelSlots = 2 * 3 * 4 * 2 * 2;
 
 int kernel_slot(int dtype, int head_dim, int block_size, int group, bool v1)
 {
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
-    const int bi = block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
-    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (group > 8 ? 1 : 0)) * 2 +
+    const int bi = block_size == 8 ? 3 : block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
+    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 2 + (group > 8 ? 1 : 0)) * 2 +
            (v1 ? 1 : 0);
 }
 
@@ -276,14 +276,14 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
 }
 
 // Per-device dynamic shared memory limit of each tcgen05 kernel after the opt-in.
-constexpr int kTcSlots = 2 * 3 * 3 * 2 * 2;
+constexpr int kTcSlots = 2 * 3 * 4 * 2 * 2;
 std::atomic<int> g_tc_smem_limit[kMaxDevices][kTcSlots];
 
 int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles)
 {
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
-    const int bi = block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
-    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 3 + bi) * 2 + (v1 ? 1 : 0)) * 2 + (tiles - 1);
+    const int bi = block_size == 8 ? 3 : block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
+    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 2 + (v1 ? 1 : 0)) * 2 + (tiles - 1);
 }
 
 // The tcgen05 kernels.  One query tile: as many K and V ring stages as keep

@@ -59,9 +59,12 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
     using E = Elem<T>;
     constexpr int kKS = D / 16;                       // 16-dim steps of Q.K, 16-dim tiles of O
     constexpr int kSlices = D / 64;                   // 64-dim slices: one TMA load each
-    constexpr uint32_t kHalfBytes = BS * 128;         // one 64-dim slice of a K or V tile
+    // A ring stage holds one "unit" of kUB blocks, at least the 16 tokens of an MMA tile.
+    constexpr int kUB = BS < 16 ? 16 / BS : 1;        // blocks per unit
+    constexpr int kUT = BS * kUB;                     // tokens per unit
+    constexpr uint32_t kHalfBytes = kUT * 128;        // one 64-dim slice of a K or V unit
     constexpr uint32_t kStageBytes = 2 * kSlices * kHalfBytes; // K slices, then V slices
-    constexpr int kTiles = BS / 16;                   // 16-row MMA tiles per block
+    constexpr int kTiles = kUT / 16;                  // 16-row MMA tiles per unit
     constexpr int kHeads = NT * 8;
     constexpr int kScr = D + 4;                       // scratch row stride (floats)
 
@@ -112,15 +115,21 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         V1 ? p.max_blocks
            : (int)min(((long long)tokA + p.partition_size + BS - 1) / BS, (long long)p.max_blocks) -
                  blk0;
-    const int cnt_max = warp < range_max ? (range_max - warp + nwarps - 1) / nwarps : 0;
-    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0 + warp;
+    const int32_t *bt_row = p.block_tables + (size_t)b * p.max_blocks + blk0;
     const int Lraw = __ldg(&p.seq_lens[b]);
-    auto load_ids = [&](int chunk, int bound) -> int32_t {
-        const int i = chunk * 32 + lane;
-        return i < bound ? __ldg(bt_row + (size_t)nwarps * i) : 0;
+    // Block ids of the warp's units (unit u = warp + nwarps * i) for i in a
+    // 32-unit chunk, one unit per lane; blocks at or past `bound` read as 0.
+    auto load_ids = [&](int chunk, int bound, int32_t(&dst)[kUB]) {
+        const int u = warp + nwarps * (chunk * 32 + lane);
+#pragma unroll
+        for (int k = 0; k < kUB; ++k) {
+            const int bi = u * kUB + k;
+            dst[k] = bi < bound ? __ldg(bt_row + bi) : 0;
+        }
     };
-    int32_t ids_cur = load_ids(0, cnt_max);
-    int32_t ids_next = load_ids(1, cnt_max);
+    int32_t ids_cur[kUB], ids_next[kUB];
+    load_ids(0, range_max, ids_cur);
+    load_ids(1, range_max, ids_next);
 
     // Q^T fragments (B operand of S^T = K Q^T): head 8j + g4, dims 16ks + 2t4 (+1, +8, +9)
     uint32_t qf[NT][kKS][2];
@@ -153,7 +162,8 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
     const int tok0 = blk0 * BS;
     const int lo = tokA - tok0;
     const int ntok = V1 ? L : (int)(min((long long)tokA + p.partition_size, (long long)L) - tok0);
-    const int nblk = (ntok + BS - 1) / BS;
+    const int nblk = (ntok + BS - 1) / BS;   // blocks of the range
+    const int nunit = (ntok + kUT - 1) / kUT; // ring stages' worth
 
     if (V1 && nblk == 0) { // empty sequence: zero output
         T *out = static_cast<T *>(p.out);
@@ -182,8 +192,8 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
     const uint32_t bar0 = smem_addr(&bars[warp * kMaxStages]);
     const int stages = p.stages;
 
-    // Blocks of this warp: j = warp + nwarps * i, i < cnt.
-    const int cnt = warp < nblk ? (nblk - warp + nwarps - 1) / nwarps : 0;
+    // Units of this warp: u = warp + nwarps * i, i < cnt.
+    const int cnt = warp < nunit ? (nunit - warp + nwarps - 1) / nwarps : 0;
 
     if (lane == 0) {
         for (int s = 0; s < stages; ++s)
@@ -200,30 +210,42 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
     int32_t status_bits = 0;
     int chunk_cur = 0;
 
-    // Issue the four TMA loads of the warp's i-th block into stage s (warp-uniform call).
+    // Issue the TMA loads of the warp's i-th unit into stage s (warp-uniform call).
     auto issue = [&](int i, int s) {
         const int c = i >> 5;
         if (c != chunk_cur) {
-            ids_cur = ids_next;
-            ids_next = load_ids(c + 1, cnt);
+#pragma unroll
+            for (int k = 0; k < kUB; ++k)
+                ids_cur[k] = ids_next[k];
+            load_ids(c + 1, nblk, ids_next);
             chunk_cur = c;
         }
-        int32_t phys = __shfl_sync(0xffffffffu, ids_cur, i & 31);
-        if (phys < 0 || phys >= p.num_blocks) {
-            status_bits |= PA_STATUS_BAD_BLOCK_ID;
-            phys = 0; // read a valid block instead of memory outside the cache
-        }
-        if (lane == 0) {
-            const uint32_t bar = bar0 + 8 * s;
-            const uint32_t dst = ring + (uint32_t)s * kStageBytes;
-            const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
-            mbar_arrive_expect_tx(bar, kStageBytes);
+        const int u = warp + nwarps * i;
+        const int nb = kUB == 1 ? 1 : min(kUB, nblk - u * kUB); // blocks in the unit
+        const uint32_t bar = bar0 + 8 * s;
+        const uint32_t dst = ring + (uint32_t)s * kStageBytes;
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, kUB == 1 ? kStageBytes : (uint32_t)nb * BS * 256u * kSlices);
 #pragma unroll
-            for (int sl = 0; sl < kSlices; ++sl)
-                tma_load_3d(dst + sl * kHalfBytes, &tmap_k, 0, sl, row, bar, policy);
+        for (int k = 0; k < kUB; ++k) {
+            int32_t phys = __shfl_sync(0xffffffffu, ids_cur[k], i & 31);
+            if (k < nb) {
+                if (phys < 0 || phys >= p.num_blocks) {
+                    status_bits |= PA_STATUS_BAD_BLOCK_ID;
+                    phys = 0; // read a valid block instead of memory outside the cache
+                }
+                if (lane == 0) {
+                    const int row = (int)(((long long)phys * p.num_kv_heads + kv) * BS);
 #pragma unroll
-            for (int sl = 0; sl < kSlices; ++sl)
-                tma_load_3d(dst + (kSlices + sl) * kHalfBytes, &tmap_v, 0, sl, row, bar, policy);
+                    for (int sl = 0; sl < kSlices; ++sl)
+                        tma_load_3d(dst + sl * kHalfBytes + k * BS * 128, &tmap_k, 0, sl, row, bar,
+                                    policy);
+#pragma unroll
+                    for (int sl = 0; sl < kSlices; ++sl)
+                        tma_load_3d(dst + (kSlices + sl) * kHalfBytes + k * BS * 128, &tmap_v, 0, sl,
+                                    row, bar, policy);
+                }
+            }
         }
     };
 
@@ -262,15 +284,16 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             status_bits |= PA_STATUS_TIMEOUT;
             break;
         }
-        const int jblk = warp + nwarps * i;
-        const int valid = min(BS, ntok - jblk * BS);
+        const int jblk = warp + nwarps * i; // unit
+        const int valid = min(kUT, ntok - jblk * kUT);
         const uint32_t kbase = ring + (uint32_t)s * kStageBytes;
         const uint32_t vbase = kbase + kSlices * kHalfBytes;
 
-        if (valid < BS) {
-            // Rows past the end of the sequence: zero V so no stale value reaches P.V.
-            // A row is kSlices lines of eight 16-byte chunks.
-            const int nchunks = (BS - valid) * kSlices * 8;
+        if (valid < kUT) {
+            // Rows past the end of the range (or of the unit's loaded blocks):
+            // zero V so no stale value reaches P.V.  A row is kSlices lines of
+            // eight 16-byte chunks.
+            const int nchunks = (kUT - valid) * kSlices * 8;
             for (int c = lane; c < nchunks; c += 32) {
                 const int r = valid + c / (kSlices * 8);
                 const int sl = (c >> 3) % kSlices;
@@ -312,7 +335,7 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             // ---- scale, mask, streaming softmax update
             // token rows of c0/c1 and (r0 + 8) of c2/c3, from tok0 + lo (an
             // unsigned compare with vis also masks the rows before lo)
-            const unsigned r0 = (unsigned)(jblk * BS + tile * 16 + g4 - lo);
+            const unsigned r0 = (unsigned)(jblk * kUT + tile * 16 + g4 - lo);
             uint32_t pb[NT][2][2]; // [n-tile][hi/lo][b0/b1]
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
@@ -384,7 +407,7 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         }
         __syncwarp();
         if (issued < cnt) {
-            if (valid < BS)
+            if (valid < kUT)
                 fence_proxy_async();
             issue(issued, s);
             ++issued;
@@ -490,6 +513,7 @@ static const void *attn_kernel_ptr(int block_size, int cols, bool v1)
         return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, true>)               \
                   : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, false>);             \
     }
+    PA_PICK(8)
     PA_PICK(16)
     PA_PICK(32)
     PA_PICK(64)

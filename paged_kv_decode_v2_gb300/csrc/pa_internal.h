@@ -53,7 +53,7 @@ struct AttnLaunch {
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
     int head_dim;                // 64, 128 or 256
-    int block_size;              // 16, 32 or 64
+    int block_size;              // 8, 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
     bool tc;                     // a tcgen05 kernel
@@ -80,10 +80,11 @@ struct MergeParams {
 };
 
 // Per-warp shared-memory ring bytes for one stage: a K tile and a V tile of
-// block_size rows x head_dim 16-bit values.
+// block_size rows (at least 16: an 8-token block size stages two blocks) x
+// head_dim 16-bit values.
 inline size_t stage_bytes(int block_size, int head_dim)
 {
-    return static_cast<size_t>(block_size) * head_dim * 4;
+    return static_cast<size_t>(block_size < 16 ? 16 : block_size) * head_dim * 4;
 }
 
 // Scratch one warp needs to hand its partial {m, l, o} to the CTA merge.

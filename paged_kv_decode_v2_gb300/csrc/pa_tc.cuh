@@ -524,12 +524,14 @@ static const void *tc_kernel_ptr(int block_size, bool v1, int tiles)
                   : reinterpret_cast<const void *>(&K<T, D, BS, false>);
     if (tiles == 2) {
         if constexpr (D <= 128) {
+            PA_PICK(tc2_attn_kernel, 8)
             PA_PICK(tc2_attn_kernel, 16)
             PA_PICK(tc2_attn_kernel, 32)
             PA_PICK(tc2_attn_kernel, 64)
         }
         return nullptr;
     }
+    PA_PICK(tc_attn_kernel, 8)
     PA_PICK(tc_attn_kernel, 16)
     PA_PICK(tc_attn_kernel, 32)
     PA_PICK(tc_attn_kernel, 64)

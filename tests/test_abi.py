@@ -80,7 +80,7 @@ def _v2(lib, **kw):
     (dict(head_dim=96), 2),
     (dict(head_dim=512), 2),
     (dict(block_size=48), 2),
-    (dict(block_size=8), 2),
+    (dict(block_size=4), 2),
     (dict(num_heads=256, num_kv_heads=2), 2),
     (dict(partition_size=-16), 1),
     (dict(partition_size=0), 1),

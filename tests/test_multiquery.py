@@ -40,7 +40,7 @@ def test_mq_rows_split_over_ctas(q_len, G):
     check_mq(wl.make_inputs(w, device="cuda"), 256)
 
 
-@pytest.mark.parametrize("D,bs", [(64, 32), (256, 16), (128, 64)])
+@pytest.mark.parametrize("D,bs", [(64, 32), (256, 16), (128, 64), (128, 8), (64, 8)])
 def test_mq_other_shapes(D, bs):
     w = mq("mq_shapes", 4, 4, (5, 130, 333), bs=bs, P=128, D=D, seed=6000 + D + bs)
     check_mq(wl.make_inputs(w, device="cuda"), 128)

@@ -50,7 +50,7 @@ def test_split_phases_equal_fused_call_bitwise():
 
 
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
-@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("bs", [8, 16, 32])
 @pytest.mark.parametrize("G", [1, 4, 8, 16])
 @pytest.mark.parametrize("P", [64, 512])
 def test_fuzz_grid(dtype, bs, G, P):
@@ -61,7 +61,7 @@ def test_fuzz_grid(dtype, bs, G, P):
 
 
 @pytest.mark.parametrize("D", [64, 256])
-@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
 @pytest.mark.parametrize("G", [1, 8, 16])
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 def test_fuzz_head_dims(D, bs, G, dtype):
@@ -83,7 +83,7 @@ def test_fuzz_block_size_64(dtype, G, P):
 
 
 @pytest.mark.parametrize("bs,P", [(16, 300), (32, 200), (64, 100), (16, 8), (32, 48), (64, 1000),
-                                  (16, 17), (32, 1)])
+                                  (16, 17), (32, 1), (8, 300), (8, 4), (8, 12)])
 @pytest.mark.parametrize("G", [4, 16])
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 def test_partition_not_a_multiple_of_block_size(bs, P, G, dtype):
@@ -111,9 +111,10 @@ def test_launch_shapes_other_head_dims(cuda_lib, D, warps, stages):
 
 
 @pytest.mark.parametrize("warps,stages", [(1, 1), (1, 2), (2, 1), (2, 4), (8, 2), (3, 3), (4, 8)])
-def test_launch_shapes_do_not_change_results(cuda_lib, warps, stages):
-    w = wl.Workload("shapes", 4, 16, 2, 128, 16, 256, wl.BF16, "list",
-                    seq_lens=(1, 700, 2049, 4096), seed=55)
+@pytest.mark.parametrize("bs", [8, 16])
+def test_launch_shapes_do_not_change_results(cuda_lib, warps, stages, bs):
+    w = wl.Workload("shapes", 4, 16, 2, 128, bs, 256, wl.BF16, "list",
+                    seq_lens=(1, 700, 2049, 4096), seed=55 + bs)
     inp = wl.make_inputs(w, device="cuda")
     cuda_lib.pa_set_launch_config(warps, stages)
     try:
@@ -147,10 +148,11 @@ def test_max_seq_len_hint():
     full_check(inp, 512, hint=1700)
 
 
-def test_unreferenced_and_tail_slots_never_reach_the_output():
-    w = wl.Workload("poison", 4, 16, 2, 128, 16, 128, wl.BF16, "list", seq_lens=(37, 16, 300, 5),
-                    seed=21)
-    inp = wl.make_inputs(w, device="cuda", max_blocks=30)
+@pytest.mark.parametrize("bs", [8, 16])
+def test_unreferenced_and_tail_slots_never_reach_the_output(bs):
+    w = wl.Workload("poison", 4, 16, 2, 128, bs, 128, wl.BF16, "list", seq_lens=(37, 16, 300, 5),
+                    seed=21 + bs)
+    inp = wl.make_inputs(w, device="cuda", max_blocks=480 // bs)
     clean = [run_v2(inp, 128, entry=e)[0] for e in ("v2", "v1")]
     wl.poison_unreferenced(inp, float("nan"))
     dirty = [run_v2(inp, 128, entry=e)[0] for e in ("v2", "v1")]

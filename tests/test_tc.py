@@ -67,7 +67,7 @@ def test_tc_single_query(G):
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
-@pytest.mark.parametrize("bs", [16, 32, 64])
+@pytest.mark.parametrize("bs", [8, 16, 32, 64])
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 def test_tc_head_dims_and_block_sizes(D, bs, dtype):
     P = 128
@@ -84,7 +84,7 @@ def test_tc_ring_stages(cuda_lib, k_stages, v_stages):
     check_mq(wl.make_inputs(w, device="cuda"), 256)
 
 
-@pytest.mark.parametrize("bs,P", [(16, 100), (32, 300), (16, 8), (64, 1000)])
+@pytest.mark.parametrize("bs,P", [(16, 100), (32, 300), (16, 8), (64, 1000), (8, 100), (8, 4)])
 def test_tc_partition_not_a_multiple_of_block_size(bs, P):
     lens = (1, 8, P - 1, P + 1, 2 * P + 7, 650)
     w = mq("tc_pnb", 8, 4, lens, bs=bs, P=P, seed=8400 + bs + P)
