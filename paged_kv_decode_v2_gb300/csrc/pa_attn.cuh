@@ -8,11 +8,12 @@
 // GQA by broadcasting the KV head instead of replicating it).
 //
 // Data movement.  Each warp of the CTA owns a private ring of `stages`
-// shared-memory stages and walks the blocks j = warp, warp + W, ... of the
-// CTA's range.  A stage holds one paged block's K tile and V tile
-// (block_size rows x head_dim each), brought in by TMA tensor loads (one per
-// 64-dim slice of K and of V) that complete on the stage's mbarrier.  The
-// block id is read from the block table a full chunk of 32 blocks ahead of
+// shared-memory stages and walks the units j = warp, warp + W, ... of the
+// CTA's range; a unit is one paged block, or two for 8-token blocks so that
+// a unit fills a 16-row MMA tile.  A stage holds a unit's K tile and V tile
+// (tokens x head_dim each), brought in by TMA tensor loads (one per block
+// and 64-dim slice of K and of V) that complete on the stage's mbarrier.
+// Block ids are read from the block table a full chunk of 32 units ahead of
 // use.  Loads use 128-byte swizzling, so the ldmatrix reads below touch 32
 // distinct banks.
 //
