@@ -17,6 +17,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import ctypes
 import json
 import math
 import os
@@ -277,7 +278,8 @@ class Decoder:
         ev[2].record()
 
     def pack_host_inputs(self):
-        """One pinned host buffer holding this step's query, block tables and lengths."""
+        """One pinned host buffer holding a step's query, block tables and lengths;
+        two device copies of it and two outputs (double buffering)."""
         inp = self.inp
         parts = [inp.query, inp.block_tables, inp.seq_lens]
         sizes = [t.numel() * t.element_size() for t in parts]
@@ -285,27 +287,120 @@ class Decoder:
         for n in sizes:
             offs.append(offs[-1] + (n + 255) // 256 * 256)
         host_in = torch.empty(offs[-1], dtype=torch.uint8).pin_memory()
-        dev_in = torch.empty(offs[-1], dtype=torch.uint8, device=self.device)
         for t, o, n in zip(parts, offs, sizes):
             host_in[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
-        views = [dev_in[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs, sizes)]
-        self.e2e_inputs = views
-        host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        return host_in, host_out, dev_in
+        self.e2e_dev_in, self.e2e_views, self.e2e_out, self.e2e_host_out = [], [], [], []
+        for _ in range(2):
+            dev_in = torch.empty(offs[-1], dtype=torch.uint8, device=self.device)
+            self.e2e_dev_in.append(dev_in)
+            self.e2e_views.append([dev_in[o:o + n].view(t.dtype).view(t.shape)
+                                   for t, o, n in zip(parts, offs, sizes)])
+            self.e2e_out.append(torch.empty_like(self.out))
+            self.e2e_host_out.append(torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory())
+        self.copy_stream = torch.cuda.Stream(device=self.device)
+        self.compute_stream = torch.cuda.Stream(device=self.device)
+        return host_in
 
-    def e2e_step(self, i: int, host_in, host_out, dev_in):
-        """Host buffers in, host result out: one H2D copy of the step's inputs, decode, D2H of out."""
+    def e2e_steps(self, k0: int, n: int, host_in):
+        """n decode steps through the C ABI with host buffers, pipelined as a
+        serving loop does: step k's inputs go host -> device on a copy stream
+        (one packed copy) while step k - 1 decodes on the compute stream, and
+        step k's `out` goes device -> host after it.  Buffers alternate between
+        two sets; every step moves its own bytes.  The copies, events and the
+        decode entry point are called through ctypes with arguments marshalled
+        once, so the host keeps ahead of the GPU.  Returns (start, end) events
+        bracketing all copies and decodes."""
+        rt, lib = _cudart(), self.pa.load()
+        cs, ks = self.copy_stream, self.compute_stream
+        csh, ksh = ctypes.c_void_p(cs.cuda_stream), ctypes.c_void_p(ks.cuda_stream)
+        if not hasattr(self, "_e2e_events"):
+            evs = []
+            for _ in range(6):
+                e = ctypes.c_void_p()
+                _rt_check(rt.cudaEventCreateWithFlags(ctypes.byref(e), 2))  # no timing
+                evs.append(e)
+            self._e2e_events = evs
+            self._e2e_args = [[self._decode_args(j, c, ksh) for c in range(self.copies)]
+                              for j in range(2)]
+        h2d_ev, dec_ev, done_ev = self._e2e_events[0:2], self._e2e_events[2:4], self._e2e_events[4:6]
+        entry = lib.pa_decode_mq if self.w.q_len > 1 else lib.pa_decode
+        nbytes_in = host_in.numel()
+        nbytes_out = self.e2e_out[0].numel() * self.e2e_out[0].element_size()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        cs.wait_stream(torch.cuda.current_stream())
+        ks.wait_stream(torch.cuda.current_stream())
+        start.record(cs)
+        for k in range(k0, k0 + n):
+            j = k % 2
+            if k - k0 >= 2:
+                _rt_check(rt.cudaStreamWaitEvent(csh, done_ev[j], 0))
+            _rt_check(rt.cudaMemcpyAsync(ctypes.c_void_p(self.e2e_dev_in[j].data_ptr()),
+                                         ctypes.c_void_p(host_in.data_ptr()), nbytes_in, 1, csh))
+            _rt_check(rt.cudaEventRecord(h2d_ev[j], csh))
+            _rt_check(rt.cudaStreamWaitEvent(ksh, h2d_ev[j], 0))
+            rc = entry(*self._e2e_args[j][k % self.copies])
+            if rc != 0:
+                raise RuntimeError(f"decode returned {rc}")
+            _rt_check(rt.cudaEventRecord(dec_ev[j], ksh))
+            _rt_check(rt.cudaStreamWaitEvent(csh, dec_ev[j], 0))
+            _rt_check(rt.cudaMemcpyAsync(ctypes.c_void_p(self.e2e_host_out[j].data_ptr()),
+                                         ctypes.c_void_p(self.e2e_out[j].data_ptr()), nbytes_out, 2,
+                                         csh))
+            _rt_check(rt.cudaEventRecord(done_ev[j], csh))
+        cs.wait_stream(ks)
+        end.record(cs)
+        return start, end
+
+    def _decode_args(self, j: int, c: int, stream):
+        """ctypes arguments of one pa_decode / pa_decode_mq call on buffer set j, cache copy c."""
         pa, w = self.pa, self.w
-        dev_in.copy_(host_in, non_blocking=True)
-        q, bt, sl = self.e2e_inputs
-        kc, vc = self.caches[i % self.copies]
+        q, bt, sl = self.e2e_views[j]
+        kc, vc = self.caches[c]
         if w.q_len > 1:
-            pa.pa_decode_mq(q, kc, vc, bt, sl, w.scale, w.partition_size, self.out, self.tmp,
-                            self.es, self.ml, max_seq_len_hint=self.max_seq_len)
+            args = pa._lib._shape_args_mq(q, kc, vc, bt, sl, self.max_seq_len, w.scale)
         else:
-            pa.pa_decode(q, kc, vc, bt, sl, w.scale, w.partition_size, self.out, self.tmp, self.es,
-                         self.ml, max_seq_len_hint=self.max_seq_len)
-        host_out.copy_(self.out, non_blocking=True)
+            args = pa._lib._shape_args(q, kc, vc, bt, sl, self.max_seq_len, w.scale)
+        return tuple(args) + (int(w.partition_size), pa._lib._DTYPE[q.dtype],
+                              ctypes.c_void_p(self.e2e_out[j].data_ptr()),
+                              ctypes.c_void_p(self.tmp.data_ptr()),
+                              ctypes.c_void_p(self.es.data_ptr()),
+                              ctypes.c_void_p(self.ml.data_ptr()), self.tmp.shape[-2], None,
+                              stream)
+
+
+_CUDART = None
+
+
+def _cudart():
+    """The CUDA runtime, for stream-ordered copies and events in the end-to-end loop."""
+    global _CUDART
+    if _CUDART is None:
+        import glob
+        cands = ["libcudart.so", "libcudart.so.13"]
+        for d in (os.environ.get("CUDA_HOME", "/usr/local/cuda"), "/usr/local/cuda"):
+            cands += sorted(glob.glob(os.path.join(d, "lib64", "libcudart.so*")))
+            cands += sorted(glob.glob(os.path.join(d, "targets", "*", "lib", "libcudart.so*")))
+        for c in cands:
+            try:
+                lib = ctypes.CDLL(c)
+                break
+            except OSError:
+                continue
+        else:
+            raise RuntimeError("libcudart not found")
+        vp, sz = ctypes.c_void_p, ctypes.c_size_t
+        lib.cudaMemcpyAsync.argtypes = [vp, vp, sz, ctypes.c_int, vp]
+        lib.cudaEventRecord.argtypes = [vp, vp]
+        lib.cudaStreamWaitEvent.argtypes = [vp, vp, ctypes.c_uint]
+        lib.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(vp), ctypes.c_uint]
+        _CUDART = lib
+    return _CUDART
+
+
+def _rt_check(rc: int):
+    if rc != 0:
+        raise RuntimeError(f"CUDA runtime error {rc}")
 
 
 def soak(dec, i0: int, seconds: float) -> int:
@@ -363,22 +458,17 @@ def time_gpu(args, w: wl.Workload):
 
     # End to end through the public API with host buffers: each step copies its
     # inputs (query, block tables, sequence lengths, packed in one pinned
-    # buffer) host -> device in one copy, decodes, and reads `out` back.
-    host_in, host_out, dev_in = dec.pack_host_inputs()
-    for i in range(W):
-        dec.e2e_step(i, host_in, host_out, dev_in)
+    # buffer) host -> device in one copy, decodes, and reads `out` back to
+    # pinned host memory; copies of one step overlap the decode of the next.
+    host_in = dec.pack_host_inputs()
+    dec.e2e_steps(0, W, host_in)
     torch.cuda.synchronize()
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for k in range(K):
-        dec.e2e_step(k, host_in, host_out, dev_in)
-    e1.record()
+    e0, e1 = dec.e2e_steps(W, K, host_in)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device) / K
     h2d = host_in.numel()
-    d2h = host_out.numel() * host_out.element_size()
+    d2h = dec.e2e_host_out[0].numel() * dec.e2e_host_out[0].element_size()
 
     gbs = world * dec.kv_bytes / (ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -416,6 +506,7 @@ def time_gpu(args, w: wl.Workload):
         },
         "e2e": {"value": round(world * dec.kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
+                "pipelined": "two buffer sets; step k's copies overlap step k +- 1's decode",
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * dec.launches_per_step,
         "roofline": ({"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2),
