@@ -3,7 +3,6 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -386,7 +385,7 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
                float *tmp_output, float *exp_sums, float *max_logits, int max_num_partitions,
                void *out, int32_t *status)
 {
-    std::memset(&L, 0, sizeof(L));
+    L = AttnLaunch{};
     int rc = encode_cache_map(&L.tmap_k, key_cache, dtype, num_blocks, num_kv_heads, block_size,
                               head_dim);
     if (rc)
