@@ -101,6 +101,26 @@ __global__ void __launch_bounds__(kTc2Threads)
     const int head = kv * p.group + ci % p.group;
     const size_t qrow = ((size_t)b * p.q_len + qi) * p.num_heads + head;
 
+    // The row's first 256 bytes of Q are fetched now, so their latency
+    // overlaps the TMEM allocation and barrier set-up below.
+    constexpr int kQChunks = D / 8;                       // 16-byte chunks of a row
+    constexpr int kEarly = kQChunks < 16 ? kQChunks : 16; // chunks held in registers
+    const uint32_t *q32 = static_cast<const uint32_t *>(p.query) + qrow * (D / 2);
+    // Rows are D * 2 bytes apart, so one base check covers every row.
+    const bool q_vec = (reinterpret_cast<uintptr_t>(p.query) & 15u) == 0;
+    auto q_chunk = [&](int ch) -> uint4 {
+        if (!row_ok)
+            return make_uint4(0u, 0u, 0u, 0u);
+        if (q_vec)
+            return __ldg(reinterpret_cast<const uint4 *>(q32) + ch);
+        return make_uint4(__ldg(q32 + ch * 4), __ldg(q32 + ch * 4 + 1), __ldg(q32 + ch * 4 + 2),
+                          __ldg(q32 + ch * 4 + 3));
+    };
+    uint4 q_early[kEarly];
+#pragma unroll
+    for (int ch = 0; ch < kEarly; ++ch)
+        q_early[ch] = q_chunk(ch);
+
     if (ntiles == 0) {
         if (row_ok) {
             if (V1) {
@@ -298,28 +318,14 @@ __global__ void __launch_bounds__(kTc2Threads)
     } else if (q < ntq) {
         // ---------------------------------------------------------- rows of tile q
         {
-            const uint32_t *q32 = static_cast<const uint32_t *>(p.query) + qrow * (D / 2);
-            const bool vec = (reinterpret_cast<uintptr_t>(p.query) & 15u) == 0;
             const uint32_t qb = q_sm + (uint32_t)q * C::kQBytes;
-#pragma unroll 4
-            for (int ch = 0; ch < D / 8; ++ch) {
-                uint32_t w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-                if (row_ok && vec) {
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q32) + ch);
-                    w0 = v.x;
-                    w1 = v.y;
-                    w2 = v.z;
-                    w3 = v.w;
-                } else if (row_ok) {
-                    w0 = __ldg(q32 + ch * 4 + 0);
-                    w1 = __ldg(q32 + ch * 4 + 1);
-                    w2 = __ldg(q32 + ch * 4 + 2);
-                    w3 = __ldg(q32 + ch * 4 + 3);
-                }
+#pragma unroll
+            for (int ch = 0; ch < kQChunks; ++ch) {
+                const uint4 v = ch < kEarly ? q_early[ch] : q_chunk(ch);
                 const uint32_t addr =
                     qb + (ch >> 3) * C::kQSlice + r * 128 + ((((ch & 7) ^ (r & 7))) << 4);
-                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w0),
-                             "r"(w1), "r"(w2), "r"(w3)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
+                             "r"(v.y), "r"(v.z), "r"(v.w)
                              : "memory");
             }
             fence_proxy_async();
