@@ -245,16 +245,27 @@ class Decoder:
         self.family = "pa_tc" if w.q_len * w.group_size >= TC_MIN_ROWS else "pa_attn"
 
     def call(self, i: int):
-        """One decode call on copy i % R through the public dispatch entry point."""
-        pa, w, inp = self.pa, self.w, self.inp
-        kc, vc = self.caches[i % self.copies]
-        if w.q_len > 1:
-            pa.pa_decode_mq(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
-                            w.partition_size, self.out, self.tmp, self.es, self.ml,
-                            max_seq_len_hint=self.max_seq_len)
-            return
-        pa.pa_decode(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, w.partition_size,
-                     self.out, self.tmp, self.es, self.ml, max_seq_len_hint=self.max_seq_len)
+        """One decode call on copy i % R through the public dispatch entry point of the
+        C ABI (pa_decode, or pa_decode_mq for several new tokens), its arguments
+        marshalled once per copy as a C caller would hold them."""
+        if not hasattr(self, "_call_args"):
+            pa, w, inp = self.pa, self.w, self.inp
+            lib = pa.load()
+            self._call_fn = lib.pa_decode_mq if w.q_len > 1 else lib.pa_decode
+            shape = pa._lib._shape_args_mq if w.q_len > 1 else pa._lib._shape_args
+            self._call_args = []
+            for kc, vc in self.caches:
+                args = shape(inp.query, kc, vc, inp.block_tables, inp.seq_lens, self.max_seq_len,
+                             w.scale)
+                self._call_args.append(tuple(args) + (
+                    int(w.partition_size), pa._lib._DTYPE[inp.query.dtype],
+                    ctypes.c_void_p(self.out.data_ptr()), ctypes.c_void_p(self.tmp.data_ptr()),
+                    ctypes.c_void_p(self.es.data_ptr()), ctypes.c_void_p(self.ml.data_ptr()),
+                    self.tmp.shape[-2], None))
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        rc = self._call_fn(*self._call_args[i % self.copies], stream)
+        if rc != 0:
+            raise RuntimeError(f"decode returned {rc}")
 
     def split_call(self, i: int, ev):
         """The same call as its kernels, with events (start, after kernel 1, end) between them."""
