@@ -18,6 +18,7 @@ constexpr int kMaxStages = 8;        // TMA ring stages per warp
 constexpr int kMergeThreads = 128;   // phase-2 CTA size
 constexpr int kTcRows = 128;         // tcgen05 kernel: query rows per CTA (the MMA's M)
 constexpr int kTcTok = 64;           // tcgen05 kernel: tokens per K/V tile
+constexpr float kTcRescaleLog2 = 8.f; // tcgen05 kernel: max P = 2^8 before m moves
 constexpr int kTcThreads = 192;      // tcgen05 kernel: 4 row warps, MMA warp, TMA warp
 constexpr int kTc2Tok = 128;         // two-tile tcgen05 kernel: tokens per K/V tile
 constexpr int kTc2Threads = 320;     // two-tile tcgen05 kernel: 8 row warps, MMA warp, TMA warp

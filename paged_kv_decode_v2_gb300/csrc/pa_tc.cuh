@@ -17,10 +17,19 @@
 //   P   = exp(S - m)      one thread per row reads its S row from TMEM,
 //                         masks, keeps the running max m and sum l, and
 //                         writes P (16-bit, split into hi + lo for bf16)
-//                         back to TMEM
+//                         back to TMEM over its S
 //   O  += P V_t           tcgen05.mma, M = 128, N = D, K = 64 tokens; A = P
 //                         in TMEM, B = V tile (MN-major) in shared memory,
-//                         O in TMEM; rescaled in place when m grows
+//                         O in TMEM
+//
+// S/P has two TMEM buffers, tile t in buffer t & 1, so the MMA thread runs
+// S of tile t + 2 right behind P.V of tile t and the rows never wait for a
+// P.V before writing their next P.  The running max m used for P and for O
+// moves only when a row's max grows by more than 2^8 in exp2 terms (P then
+// stays <= 2^8, exactly representable scaling, no loss of precision); O is
+// rescaled, after waiting for the last P.V, only then.  O / l does not depend
+// on which m was used.  The true max is tracked beside it, and a V2 partial
+// reports that max with l rescaled to it, as the merge expects.
 //
 // Warp roles: warps 0-3 own the 128 rows (softmax, epilogue), warp 4 issues
 // the MMAs (one thread) and owns the TMEM allocation, two lanes of warp 5
@@ -42,10 +51,10 @@ struct TcCfg {
     static constexpr uint32_t kKVSlice = kTcTok * 128;              // bytes of one K or V slice
     static constexpr uint32_t kQBytes = kQSlice * kSlices;
     static constexpr uint32_t kKVBytes = kKVSlice * kSlices;        // one K (or V) tile
-    // TMEM columns: O at [0, D), S at [D, D + 64), P hi at [D + 64, D + 96)
-    // and P lo at [D + 96, D + 128) (two 16-bit values per column).
+    // TMEM columns: O at [0, D), S/P buffer j at [D + 64 j, D + 64 j + 64).
+    // P is written over its S: hi at the buffer's first 32 columns, lo at
+    // the next 32 (two 16-bit values per column).
     static constexpr uint32_t kSCol = D;
-    static constexpr uint32_t kPCol = D + kTcTok;
     static constexpr uint32_t kCols = D + 2 * kTcTok <= 256 ? 256 : 512;
 };
 
@@ -61,7 +70,7 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
 
     __shared__ uint64_t k_full[kMaxStages], v_full[kMaxStages], k_empty[kMaxStages],
         v_empty[kMaxStages];
-    __shared__ uint64_t q_full, s_full, s_free, p_full, o_done, drained;
+    __shared__ uint64_t q_full, s_full[2], p_full[2], o_done[2], drained;
     __shared__ uint32_t tmem_base_sh;
     __shared__ int abort_sh;
     extern __shared__ uint8_t dyn_smem[];
@@ -158,9 +167,9 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     const uint32_t v_sm = k_sm + (uint32_t)kst * C::kKVBytes;
     const uint32_t b_k_full = smem_addr(k_full), b_v_full = smem_addr(v_full);
     const uint32_t b_k_empty = smem_addr(k_empty), b_v_empty = smem_addr(v_empty);
-    const uint32_t b_q_full = smem_addr(&q_full), b_s_full = smem_addr(&s_full);
-    const uint32_t b_s_free = smem_addr(&s_free), b_p_full = smem_addr(&p_full);
-    const uint32_t b_o_done = smem_addr(&o_done), b_drained = smem_addr(&drained);
+    const uint32_t b_q_full = smem_addr(&q_full), b_s_full = smem_addr(s_full);
+    const uint32_t b_p_full = smem_addr(p_full), b_o_done = smem_addr(o_done);
+    const uint32_t b_drained = smem_addr(&drained);
     volatile int *abort_flag = &abort_sh;
 
     if (warp == 4) {
@@ -177,10 +186,11 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             mbar_init(b_v_empty + 8 * s, 1);
         }
         mbar_init(b_q_full, kTcRows);
-        mbar_init(b_s_full, 1);
-        mbar_init(b_s_free, kTcRows);
-        mbar_init(b_p_full, kTcRows);
-        mbar_init(b_o_done, 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(b_s_full + 8 * j, 1);
+            mbar_init(b_p_full + 8 * j, kTcRows);
+            mbar_init(b_o_done + 8 * j, 1);
+        }
         mbar_init(b_drained, 1);
         abort_sh = 0;
         mbar_init_fence();
@@ -227,14 +237,14 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             };
             fetch(0, nxt);
             int issued = 0;
+            int s = 0;         // ring stage of tile t
+            uint32_t ph = 0u;  // its fill round & 1
             for (int t = 0; t < ntiles; ++t) {
 #pragma unroll
                 for (int k = 0; k < kBPT; ++k)
                     ids[k] = nxt[k];
                 fetch(t + 1, nxt);
-                const int s = t % stages;
-                if (t >= stages &&
-                    !mbar_wait_abortable(empty + 8 * s, (uint32_t)((t / stages) - 1) & 1u, abort_flag)) {
+                if (t >= stages && !mbar_wait_abortable(empty + 8 * s, ph ^ 1u, abort_flag)) {
                     status_bits |= PA_STATUS_TIMEOUT;
                     *abort_flag = 1;
                     break;
@@ -252,6 +262,10 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                     }
                 }
                 issued = t + 1;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             // Let copies still in flight land before the CTA's shared memory
             // is released (they have normally been consumed long ago).
@@ -261,58 +275,70 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
         __syncwarp();
     } else if (warp == 4) {
         // ---------------------------------------------------------- MMA issuer
+        // Order: S(0), S(1), then per tile P.V(t) followed by S(t + 2) into
+        // the buffer P(t) occupied.  tcgen05 MMAs of one thread run in issue
+        // order, so S(t + 2) overwrites P(t) only after P.V(t) has read it,
+        // and a commit that S(t) signals also covers every earlier P.V.
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16<kBf16>(kTcRows, kTcTok, false);
             constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
-            auto issue_s = [&](int t) {
-                const uint32_t kb = k_sm + (uint32_t)(t % kst) * C::kKVBytes;
+            // Descriptors are linear in the address (start / 16 in the low
+            // bits, shared memory < 256 KB): offsets are added to a base.
+            const uint64_t qd = smem_desc_sw128(q_sm, 16, 1024);
+            const uint64_t kd = smem_desc_sw128(k_sm, 16, 1024);
+            const uint64_t vd = smem_desc_sw128(v_sm, C::kKVSlice, 1024);
+            int ks_next = 0;       // K ring stage of the next S
+            uint32_t kph = 0u;     // and its fill round & 1
+            // S(t) into buffer t & 1 once K tile t has landed.
+            auto issue_s = [&](int t) -> bool {
+                if (!mbar_wait_abortable(b_k_full + 8 * ks_next, kph, abort_flag))
+                    return false;
+                tc_fence_after();
+                const uint32_t sc = tmem + C::kSCol + (uint32_t)(t & 1) * kTcTok;
+                const uint64_t kb = kd + (((uint32_t)ks_next * C::kKVBytes) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t sl = ks >> 2, kk = (ks & 3) * 32;
-                    tc_mma_ss(tmem + C::kSCol, smem_desc_sw128(q_sm + sl * C::kQSlice + kk, 16, 1024),
-                              smem_desc_sw128(kb + sl * C::kKVSlice + kk, 16, 1024), idesc_s,
-                              ks > 0);
+                    const uint32_t off_q = (ks >> 2) * C::kQSlice + (ks & 3) * 32;
+                    const uint32_t off_k = (ks >> 2) * C::kKVSlice + (ks & 3) * 32;
+                    tc_mma_ss(sc, qd + (off_q >> 4), kb + (off_k >> 4), idesc_s, ks > 0);
                 }
-                tc_commit(b_s_full);
-                tc_commit(b_k_empty + 8 * (t % kst));
+                tc_commit(b_s_full + 8 * (t & 1));
+                tc_commit(b_k_empty + 8 * ks_next);
+                if (++ks_next == kst) {
+                    ks_next = 0;
+                    kph ^= 1u;
+                }
+                return true;
             };
-            bool ok = mbar_wait_abortable(b_q_full, 0, abort_flag) &&
-                      mbar_wait_abortable(b_k_full, 0, abort_flag);
-            if (ok) {
-                tc_fence_after();
-                issue_s(0);
-            }
+            bool ok = mbar_wait_abortable(b_q_full, 0, abort_flag) && issue_s(0) &&
+                      (ntiles == 1 || issue_s(1));
+            int vs = 0;            // V ring stage of tile t
+            uint32_t vph = 0u;
             for (int t = 0; ok && t < ntiles; ++t) {
-                const int s = t % vst;
-                if (t + 1 < ntiles) {
-                    const int s1 = (t + 1) % kst;
-                    ok = mbar_wait_abortable(b_s_free, (uint32_t)t & 1u, abort_flag) &&
-                         mbar_wait_abortable(b_k_full + 8 * s1, (uint32_t)((t + 1) / kst) & 1u,
-                                             abort_flag);
-                    if (!ok)
-                        break;
-                    tc_fence_after();
-                    issue_s(t + 1);
-                }
-                ok = mbar_wait_abortable(b_p_full, (uint32_t)t & 1u, abort_flag) &&
-                     mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u, abort_flag);
+                const uint32_t pc = tmem + C::kSCol + (uint32_t)(t & 1) * kTcTok;
+                ok = mbar_wait_abortable(b_p_full + 8 * (t & 1), (uint32_t)(t >> 1) & 1u, abort_flag) &&
+                     mbar_wait_abortable(b_v_full + 8 * vs, vph, abort_flag);
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t vb = v_sm + (uint32_t)s * C::kKVBytes;
+                const uint64_t vb = vd + (((uint32_t)vs * C::kKVBytes) >> 4);
 #pragma unroll
                 for (int kt = 0; kt < kTcTok / 16; ++kt)
-                    tc_mma_ts(tmem, tmem + C::kPCol + kt * 8,
-                              smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024), idesc_o,
+                    tc_mma_ts(tmem, pc + kt * 8, vb + ((kt * 2048) >> 4), idesc_o,
                               (t > 0 || kt > 0) ? 1u : 0u);
                 if (kBf16) {
 #pragma unroll
                     for (int kt = 0; kt < kTcTok / 16; ++kt)
-                        tc_mma_ts(tmem, tmem + C::kPCol + 32 + kt * 8,
-                                  smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024), idesc_o, 1u);
+                        tc_mma_ts(tmem, pc + 32 + kt * 8, vb + ((kt * 2048) >> 4), idesc_o, 1u);
                 }
-                tc_commit(b_o_done);
-                tc_commit(b_v_empty + 8 * s);
+                tc_commit(b_o_done + 8 * (t & 1));
+                tc_commit(b_v_empty + 8 * vs);
+                if (++vs == vst) {
+                    vs = 0;
+                    vph ^= 1u;
+                }
+                if (t + 2 < ntiles)
+                    ok = issue_s(t + 2);
             }
             if (!ok) {
                 status_bits |= PA_STATUS_TIMEOUT;
@@ -345,22 +371,23 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
         const unsigned span = (unsigned)max(hi - tokA, 0);
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         const float scale = p.scale;
-        float m_run = -INFINITY, l_run = 0.f;
+        // m_run: the max P and O are relative to; m_true: the row's max.
+        float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
+            const uint32_t sc = lane_base + C::kSCol + (uint32_t)(t & 1) * kTcTok;
             // Waits end in a warp-uniform decision: tcgen05.ld / st are warp-collective.
-            if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full, (uint32_t)t & 1u, abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full + 8 * (t & 1),
+                                                             (uint32_t)(t >> 1) & 1u, abort_flag))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32_async(lane_base + C::kSCol, sr[0]);
-            tmem_ld32_async(lane_base + C::kSCol + 32, sr[1]);
+            tmem_ld32_async(sc, sr[0]);
+            tmem_ld32_async(sc + 32, sr[1]);
             tmem_ld_wait(sr[0]);
             tmem_ld_wait(sr[1]);
-            tc_fence_before();
-            mbar_arrive(b_s_free);
 
             const int off = tok0 + t * kTcTok - tokA; // token (t's first) - tokA
             // x: the exp2 argument is x * cf - mb.  On a tile every row of the
@@ -388,34 +415,24 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
                 cf = kLog2e;
             }
-            const float mn = fmaxf(m_run, mx);
-            // A row with no visible token yet (max still -inf) keeps l = o = 0.
-            const float a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
-            const float mb = mn != -INFINITY ? mn * kLog2e : 0.f;
-            uint32_t ph[32], pl[32];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < kTcTok; c += 2) {
-                const float p0 = fast_exp2(fmaf(x[c], cf, -mb));
-                const float p1 = fast_exp2(fmaf(x[c + 1], cf, -mb));
-                ls[(c >> 1) & 3] += p0 + p1;
-                const uint32_t h = E::pack(p0, p1);
-                ph[c >> 1] = h;
-                pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
-            }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l_run = fmaf(l_run, a, lsum);
-            m_run = mn;
-
-            // O and the P columns are free once the previous P.V has completed.
-            if (t > 0) {
-                if (!__all_sync(0xffffffffu,
-                                mbar_wait_abortable(b_o_done, (uint32_t)(t - 1) & 1u, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, a != 1.f)) {
+            m_true = fmaxf(m_true, mx);
+            // Move m when a row of the warp would otherwise see P > 2^8 (the
+            // first visible tile always: m_run = -inf).  NaN (both -inf) is no.
+            float a = 1.f;
+            if (__any_sync(0xffffffffu, (mx - m_run) * kLog2e > kTcRescaleLog2)) {
+                const float mn = fmaxf(m_run, mx);
+                // A row with no visible token yet (max still -inf) keeps l = o = 0.
+                a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
+                m_run = mn;
+                // O is rescaled once the last P.V has landed (tile 0 has no O yet).
+                if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
+                                                        (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
 #pragma unroll 1
                     for (int cc = 0; cc < D; cc += 64) {
                         uint32_t o0[32], o1[32];
@@ -432,10 +449,27 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                     }
                 }
             }
+            const float mb = m_run != -INFINITY ? m_run * kLog2e : 0.f;
+            uint32_t ph[32], pl[32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < kTcTok; c += 2) {
+                const float p0 = fast_exp2(fmaf(x[c], cf, -mb));
+                const float p1 = fast_exp2(fmaf(x[c + 1], cf, -mb));
+                ls[(c >> 1) & 3] += p0 + p1;
+                const uint32_t h = E::pack(p0, p1);
+                ph[c >> 1] = h;
+                pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
+            }
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l_run = fmaf(l_run, a, lsum);
+
+            // P over S in the same buffer: its S was read above, and P.V(t - 2),
+            // the last reader of the buffer, completed before S(t) did.
             if (kBf16)
-                tmem_st32x2(lane_base + C::kPCol, ph, lane_base + C::kPCol + 32, pl);
+                tmem_st32x2(sc, ph, sc + 32, pl);
             else
-                tmem_st32(lane_base + C::kPCol, ph);
+                tmem_st32(sc, ph);
 
             if (t == ntiles - 1) {
                 // Tile rows past the range (unloaded blocks, slots past the
@@ -444,6 +478,17 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 const int vt = tokE - (tok0 + t * kTcTok);
                 if (vt < kTcTok) {
                     const int s = t % vst;
+                    // The parity wait for V(t) is unambiguous once the stage's
+                    // previous fill, V(t - vst), has landed.  S(t) followed
+                    // P.V(t - 2), so that holds for vst >= 2; a one-stage ring
+                    // waits for P.V(t - 1) first.
+                    if (vst == 1 && t > 0 &&
+                        !__all_sync(0xffffffffu,
+                                    mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
+                                                        (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
                     if (!__all_sync(0xffffffffu,
                                     mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u,
                                                         abort_flag))) {
@@ -461,10 +506,13 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(b_p_full);
+            mbar_arrive(b_p_full + 8 * (t & 1));
         }
-        if (ok && !__all_sync(0xffffffffu, mbar_wait_abortable(b_o_done, (uint32_t)(ntiles - 1) & 1u,
-                                                               abort_flag)))
+        // P.V(ntiles - 1), the last MMA; P.V(ntiles - 3) completed before
+        // S(ntiles - 1), so the parity wait cannot be a phase early.
+        if (ok && !__all_sync(0xffffffffu,
+                              mbar_wait_abortable(b_o_done + 8 * ((ntiles - 1) & 1),
+                                                  (uint32_t)((ntiles - 1) >> 1) & 1u, abort_flag)))
             ok = false;
         if (!ok) {
             status_bits |= PA_STATUS_TIMEOUT;
@@ -502,8 +550,10 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                     }
                 }
                 if (row_ok) {
-                    p.exp_sums[slot] = l_run;
-                    p.max_logits[slot] = m_run;
+                    // The partition's statistics relative to its true max.
+                    p.exp_sums[slot] =
+                        m_true != -INFINITY ? l_run * fast_exp2((m_run - m_true) * kLog2e) : 0.f;
+                    p.max_logits[slot] = m_true;
                 }
             }
         }
