@@ -15,7 +15,10 @@
 //     computed from, so the next S of that tile is issued right after its
 //     P.V, in order on the tensor pipe;
 //   * the MMA thread alternates the tiles: while one tile's rows run their
-//     softmax, the tensor cores run the other tile's P.V and next S.
+//     softmax, the tensor cores run the other tile's P.V and next S;
+//   * as in pa_tc.cuh, the running max m moves only when a row would
+//     otherwise see P > 2^8, so O is rarely rescaled; a V2 partial reports
+//     the true max with l rescaled to it.
 //
 // Warp roles: warps 0-3 own the rows of tile 0 and warps 4-7 those of tile
 // 1 (one row per thread), warp 8 issues the MMAs and owns the TMEM
@@ -213,14 +216,14 @@ __global__ void __launch_bounds__(kTc2Threads)
             };
             fetch(0, nxt);
             int issued = 0;
+            int s = 0;         // ring stage of tile t
+            uint32_t ph = 0u;  // its fill round & 1
             for (int t = 0; t < ntiles; ++t) {
 #pragma unroll
                 for (int k = 0; k < kBPT; ++k)
                     ids[k] = nxt[k];
                 fetch(t + 1, nxt);
-                const int s = t % stages;
-                if (t >= stages &&
-                    !mbar_wait_abortable(empty + 8 * s, (uint32_t)((t / stages) - 1) & 1u, abort_flag)) {
+                if (t >= stages && !mbar_wait_abortable(empty + 8 * s, ph ^ 1u, abort_flag)) {
                     status_bits |= PA_STATUS_TIMEOUT;
                     *abort_flag = 1;
                     break;
@@ -238,6 +241,10 @@ __global__ void __launch_bounds__(kTc2Threads)
                     }
                 }
                 issued = t + 1;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             for (int t = max(0, issued - stages); t < issued; ++t)
                 mbar_wait_bounded(full + 8 * (t % stages), (uint32_t)(t / stages) & 1u, kWaitLimitNs);
@@ -248,27 +255,33 @@ __global__ void __launch_bounds__(kTc2Threads)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16<kBf16>(kTcRows, kTc2Tok, false);
             constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
-            // S_q(t) = Q_q K_t^T into tile q's S columns.
-            auto issue_s = [&](int qq, int t) {
-                const uint32_t kb = k_sm + (uint32_t)(t % kst) * C::kKVBytes;
-                const uint32_t qb = q_sm + (uint32_t)qq * C::kQBytes;
+            // Descriptors are linear in the address (start / 16 in the low
+            // bits, shared memory < 256 KB): offsets are added to a base.
+            const uint64_t qd = smem_desc_sw128(q_sm, 16, 1024);
+            const uint64_t kd = smem_desc_sw128(k_sm, 16, 1024);
+            const uint64_t vd = smem_desc_sw128(v_sm, C::kKVSlice, 1024);
+            // S_q = Q_q K^T of the K tile in ring stage ks into tile q's S columns.
+            auto issue_s = [&](int qq, int ks_stage) {
+                const uint64_t kb = kd + (((uint32_t)ks_stage * C::kKVBytes) >> 4);
+                const uint64_t qb = qd + (((uint32_t)qq * C::kQBytes) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t sl = ks >> 2, kk = (ks & 3) * 32;
-                    tc_mma_ss(tmem + qq * C::kTileCols + C::kSCol,
-                              smem_desc_sw128(qb + sl * C::kQSlice + kk, 16, 1024),
-                              smem_desc_sw128(kb + sl * C::kKVSlice + kk, 16, 1024), idesc_s, ks > 0);
+                    const uint32_t off_q = (ks >> 2) * C::kQSlice + (ks & 3) * 32;
+                    const uint32_t off_k = (ks >> 2) * C::kKVSlice + (ks & 3) * 32;
+                    tc_mma_ss(tmem + qq * C::kTileCols + C::kSCol, qb + (off_q >> 4), kb + (off_k >> 4),
+                              idesc_s, ks > 0);
                 }
             };
-            // O_q += P_q V_t: P's 16 tokens of K-step kt sit at S column
-            // 32 (kt / 2) + 8 (kt % 2), the lo halves 16 columns further.
-            auto issue_pv = [&](int qq, int t) {
-                const uint32_t vb = v_sm + (uint32_t)(t % vst) * C::kKVBytes;
+            // O_q += P_q V of tile t in ring stage vs_stage: P's 16 tokens of
+            // K-step kt sit at S column 32 (kt / 2) + 8 (kt % 2), the lo
+            // halves 16 columns further.
+            auto issue_pv = [&](int qq, int vs_stage, int t) {
+                const uint64_t vb = vd + (((uint32_t)vs_stage * C::kKVBytes) >> 4);
                 const uint32_t pc = tmem + qq * C::kTileCols + C::kSCol;
 #pragma unroll
                 for (int kt = 0; kt < kTc2Tok / 16; ++kt) {
                     const uint32_t a = pc + 32 * (kt >> 1) + 8 * (kt & 1);
-                    const uint64_t bd = smem_desc_sw128(vb + kt * 2048, C::kKVSlice, 1024);
+                    const uint64_t bd = vb + ((kt * 2048) >> 4);
                     tc_mma_ts(tmem + qq * C::kTileCols, a, bd, idesc_o, (t > 0 || kt > 0) ? 1u : 0u);
                     if (kBf16)
                         tc_mma_ts(tmem + qq * C::kTileCols, a + 16, bd, idesc_o, 1u);
@@ -284,28 +297,39 @@ __global__ void __launch_bounds__(kTc2Threads)
                 }
                 tc_commit(b_k_empty);
             }
+            int vs = 0;                          // V ring stage of tile t
+            uint32_t vph = 0u;                   // and its fill round & 1
+            int ks1 = kst > 1 ? 1 : 0;           // K ring stage of tile t + 1
+            uint32_t kph1 = kst > 1 ? 0u : 1u;
             for (int t = 0; ok && t < ntiles; ++t) {
-                ok = mbar_wait_abortable(b_v_full + 8 * (t % vst), (uint32_t)(t / vst) & 1u, abort_flag);
+                ok = mbar_wait_abortable(b_v_full + 8 * vs, vph, abort_flag);
                 for (int qq = 0; ok && qq < ntq; ++qq) {
                     ok = mbar_wait_abortable(b_p_full + 8 * qq, (uint32_t)t & 1u, abort_flag);
                     if (ok && qq == 0 && t + 1 < ntiles)
-                        ok = mbar_wait_abortable(b_k_full + 8 * ((t + 1) % kst),
-                                                 (uint32_t)((t + 1) / kst) & 1u, abort_flag);
+                        ok = mbar_wait_abortable(b_k_full + 8 * ks1, kph1, abort_flag);
                     if (!ok)
                         break;
                     tc_fence_after();
-                    issue_pv(qq, t);
+                    issue_pv(qq, vs, t);
                     if (t + 1 < ntiles)
-                        issue_s(qq, t + 1);
+                        issue_s(qq, ks1);
                     // Arrives once P.V(t) and S(t + 1) of tile qq are done (the
                     // last tile: once its final P.V is).
                     tc_commit(b_s_full + 8 * qq);
                 }
                 if (!ok)
                     break;
-                tc_commit(b_v_empty + 8 * (t % vst));
+                tc_commit(b_v_empty + 8 * vs);
                 if (t + 1 < ntiles)
-                    tc_commit(b_k_empty + 8 * ((t + 1) % kst));
+                    tc_commit(b_k_empty + 8 * ks1);
+                if (++vs == vst) {
+                    vs = 0;
+                    vph ^= 1u;
+                }
+                if (++ks1 == kst) {
+                    ks1 = 0;
+                    kph1 ^= 1u;
+                }
             }
             if (!ok) {
                 status_bits |= PA_STATUS_TIMEOUT;
@@ -338,7 +362,8 @@ __global__ void __launch_bounds__(kTc2Threads)
         const uint32_t s_col = o_col + C::kSCol;
         const uint32_t b_sf = b_s_full + 8 * q, b_pf = b_p_full + 8 * q;
         const float scale = p.scale;
-        float m_run = -INFINITY, l_run = 0.f;
+        // m_run: the max P and O are relative to; m_true: the row's max.
+        float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             // S_q(t) is ready, and P.V of the previous tile is done (O is stable).
@@ -382,9 +407,16 @@ __global__ void __launch_bounds__(kTc2Threads)
                 mx *= scale;
                 cf = scale * kLog2e;
             }
-            const float mn = fmaxf(m_run, mx);
-            const float a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
-            const float mb = mn != -INFINITY ? mn * kLog2e : 0.f;
+            m_true = fmaxf(m_true, mx);
+            // m moves only when a row of the warp would otherwise see P > 2^8
+            // (always on its first visible tile, where m_run = -inf).
+            float a = 1.f;
+            if (__any_sync(0xffffffffu, (mx - m_run) * kLog2e > kTcRescaleLog2)) {
+                const float mn = fmaxf(m_run, mx);
+                a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
+                m_run = mn;
+            }
+            const float mb = m_run != -INFINITY ? m_run * kLog2e : 0.f;
             // Pass 2, 64 tokens at a time: P = exp(x * cf - mb), written over
             // the S columns just read: per 32 tokens, hi halves at [32k, 32k +
             // 16), lo at [32k + 16, 32k + 32).
@@ -427,8 +459,7 @@ __global__ void __launch_bounds__(kTc2Threads)
                 }
             }
             l_run = fmaf(l_run, a, (ls[0] + ls[1]) + (ls[2] + ls[3]));
-            m_run = mn;
-            // Rescale O when the max grew (O holds P.V of earlier tiles only from t = 1).
+            // Rescale O when m moved (O holds P.V of earlier tiles only from t = 1).
             if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
 #pragma unroll 1
                 for (int cc = 0; cc < D; cc += 64) {
@@ -510,8 +541,10 @@ __global__ void __launch_bounds__(kTc2Threads)
                     }
                 }
                 if (row_ok) {
-                    p.exp_sums[slot] = l_run;
-                    p.max_logits[slot] = m_run;
+                    // The partition's statistics relative to its true max.
+                    p.exp_sums[slot] =
+                        m_true != -INFINITY ? l_run * fast_exp2((m_run - m_true) * kLog2e) : 0.f;
+                    p.max_logits[slot] = m_true;
                 }
             }
         }
