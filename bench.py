@@ -46,6 +46,7 @@ KERNEL_SOURCES = {
     "pa_attn": ["paged_kv_decode_v2_gb300/csrc/pa_attn.cuh",
                 "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
     "pa_tc": ["paged_kv_decode_v2_gb300/csrc/pa_tc.cuh",
+              "paged_kv_decode_v2_gb300/csrc/pa_tc2.cuh",
               "paged_kv_decode_v2_gb300/csrc/pa_tcgen05.cuh",
               "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
 }

@@ -277,8 +277,9 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
  * process-wide: 0 (default) picks by row count -- up to 63 rows the
  * mma.sync kernel (16 rows per CTA), from 64 rows a tcgen05 kernel (128-row
  * query tiles, S and O accumulated in tensor memory; two tiles sharing each
- * K/V tile per CTA when a KV head has more than 128 rows and head_dim <=
- * 128); 1 always the mma.sync kernel; 2 always a tcgen05 kernel; 3 always
+ * K/V tile per CTA for fp16 when a KV head has more than 128 rows, head_dim
+ * <= 128 and sequences reach 1024 tokens, else one tile and two CTAs per
+ * SM); 1 always the mma.sync kernel; 2 always a tcgen05 kernel; 3 always
  * the one-tile tcgen05 kernel; 4 always the two-tile one (one tile for
  * head_dim 256).  Either kernel computes the same
  * result within the stated tolerances; the choice changes only speed.  The

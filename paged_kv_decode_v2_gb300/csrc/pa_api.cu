@@ -357,21 +357,32 @@ bool use_tc(int cols)
     return mode >= 2 || (mode == 0 && cols >= kTcMinRows);
 }
 
-// 128-row query tiles per CTA of the tcgen05 kernel: two when a KV head has
-// more than 128 rows and two tiles' O and S fit the SM's 512 TMEM columns.
-int tc_tiles(int cols, int head_dim)
+// 128-row query tiles per CTA of the tcgen05 kernel.  Two tiles (one CTA per
+// SM, two tiles' O and S in the SM's 512 TMEM columns, each K/V tile shared)
+// need head_dim <= 128.  By default they are taken for fp16 when a KV head
+// has more than 128 rows and sequences reach 1024 tokens; bf16, whose split
+// P doubles the P.V work, and short sequences run faster with one tile and
+// two CTAs per SM.  Measured on GB300 (V1, one vs two tiles): chunked prefill
+// (2 x 2048 new tokens after 30K) bf16 2384 vs 2495 us, fp16 2137 vs 1903;
+// 4 x 1024 new after 3072 bf16 323 vs 351, fp16 296 vs 282; 8 x 512 new
+// tokens, no prefix, fp16 75 vs 87.
+int tc_tiles(int cols, int head_dim, int dtype, int max_seq_len)
 {
     const int mode = g_rows_kernel.load(std::memory_order_relaxed);
     if (head_dim > 128 || mode == 3)
         return 1;
-    return (mode == 4 || cols > kTcRows) ? 2 : 1;
+    if (mode == 4)
+        return 2;
+    return (dtype == PA_F16 && cols > kTcRows && max_seq_len >= 1024) ? 2 : 1;
 }
 
 // CTAs that split the query rows of one KV head and range.
-int row_ctas(int cols, int head_dim)
+int row_ctas(int cols, int head_dim, int dtype, int max_seq_len)
 {
-    if (use_tc(cols))
-        return (cols + kTcRows * tc_tiles(cols, head_dim) - 1) / (kTcRows * tc_tiles(cols, head_dim));
+    if (use_tc(cols)) {
+        const int rows = kTcRows * tc_tiles(cols, head_dim, dtype, max_seq_len);
+        return (cols + rows - 1) / rows;
+    }
     return cols <= 8 ? 1 : (cols + kMaxGroup - 1) / kMaxGroup;
 }
 
@@ -407,8 +418,8 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     if (L.tc) {
         // 128 rows per query tile; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
-        L.tc_tiles = tc_tiles(p.cols, head_dim);
-        p.col_groups = row_ctas(p.cols, head_dim);
+        L.tc_tiles = tc_tiles(p.cols, head_dim, dtype, cap);
+        p.col_groups = row_ctas(p.cols, head_dim, dtype, cap);
     } else {
         // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
         L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
@@ -545,16 +556,20 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 // already gives every SM a CTA and a KV head has at least 16 query rows, so
 // each CTA carries enough work; otherwise V2.  Measured on GB300, batch
 // decode (32 seqs up to 8192 tokens, 32 / 8 heads) checking q_len tokens:
-// q_len 2: V2 92 vs V1 100 us; 4: V1 113 vs 123; 8: V1 157 vs 223; 32: V1
-// 230 vs 289; 100K-token sequence, q_len 16: V2 103 vs V1 2229 us; chunked
-// prefill (2 x 2048 new tokens after 30K): V1 3579 vs V2 6129 us.
+// q_len 2: V2 92 vs V1 100 us; 4: V1 113 vs 123; 8: V1 157 vs 223; 16: V1
+// 178 vs 188; 32: V1 173 vs 235; 100K-token sequence, q_len 16: V2 87 vs V1
+// 1615 us; chunked prefill (2 x 2048 new tokens after 30K): V1 2384 vs V2
+// 4867 us.
 int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int head_dim,
                       int max_seq_len, int partition_size, int sms)
 {
     if (pa_v2_num_partitions(max_seq_len, partition_size) <= 1)
         return 1;
     const int cols = q_len * group;
-    const long long ctas = (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim);
+    // Counted with one query tile per CTA (the bf16 choice; fp16 may pair
+    // tiles, which happens only for many-row steps that fill the GPU anyway).
+    const long long ctas =
+        (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim, PA_BF16, max_seq_len);
     return (cols >= 16 && ctas >= sms) ? 1 : 2;
 }
 
