@@ -32,6 +32,15 @@ def test_mq_fuzz(q_len, G, dtype):
     check_mq(wl.make_inputs(w, device="cuda"), P)
 
 
+@pytest.mark.parametrize("G", [1, 8])
+def test_mq_empty_sequences_mixed_in(G):
+    """Zero-length sequences between others: V1 writes zero rows, V2 no partition and the merge
+    zero rows (the mma.sync kernel: q_len * G < 64)."""
+    w = mq("mq_empty", 4, G, (0, 70, 0, 2, 500, 0), P=64, seed=4500 + G)
+    ref = check_mq(wl.make_inputs(w, device="cuda"), 64)
+    assert (ref[0] == 0).all() and (ref[2] == 0).all() and (ref[5] == 0).all()
+
+
 @pytest.mark.parametrize("q_len,G", [(4, 8), (8, 4), (3, 16), (64, 1), (16, 8)])
 def test_mq_rows_split_over_ctas(q_len, G):
     """More than 16 query rows per KV head: rows split over side-by-side CTAs."""

@@ -134,6 +134,35 @@ def test_tc_rising_and_falling_scores(c, period):
     check_mq(inp, 256)
 
 
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_empty_sequences_mixed_in(dtype):
+    """Zero-length sequences between others (and a sequence shorter than q_len): V1 writes zero
+    rows for them, V2 writes no partition and the merge zero rows."""
+    lens = (0, 300, 0, 5, 1200, 0)
+    w = mq("tc_empty", 16, 8, lens, P=256, dtype=dtype, seed=9000 + dtype)
+    inp = wl.make_inputs(w, device="cuda")
+    ref = check_mq(inp, 256)
+    assert (ref[0] == 0).all() and (ref[2] == 0).all() and (ref[5] == 0).all()
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_maximum_q_len(dtype):
+    """q_len 4096, the largest the entry points take: 4096 new tokens after a 100-token prefix, one
+    query head per KV head (4096 rows per KV head), sampled rows (first, last, tile and partition
+    edges) of both heads, V1 and V2, against the oracle."""
+    Q = 4096
+    w = mq("tc_qmax", Q, 1, (Q + 100,), P=512, dtype=dtype, seed=9100 + dtype)
+    inp = wl.make_inputs(w, device="cuda")
+    prob = oracle_problem(inp)
+    rows = [0, 1, 127, 128, 411, 412, 2047, 2048, Q - 129, Q - 1]
+    pairs = [(r, h) for r in rows for h in range(w.num_heads)]
+    ref = oracle.decode(prob, pairs=pairs)
+    for e in ("v1", "v2"):
+        out = run_mq(inp, 512, entry=e)[0]
+        g = torch.stack([out[r // Q, r % Q, h] for r, h in pairs])
+        check_out(g, ref, w.dtype, what=f"{w.name}/{e}")
+
+
 def test_tc_agrees_with_the_mma_sync_kernel(cuda_lib):
     """Both kernels on the same inputs, each against the oracle and against the other."""
     w = mq("tc_vs_mma", 8, 4, (3, 100, 513, 900), P=256, seed=8600)
