@@ -315,26 +315,27 @@ class Decoder:
 
     def e2e_steps(self, k0: int, n: int, host_in):
         """n decode steps through the C ABI with host buffers, pipelined as a
-        serving loop does: step k's inputs go host -> device on a copy stream
-        (one packed copy) while step k - 1 decodes on the compute stream, and
-        step k's `out` goes device -> host after it.  Buffers alternate between
-        two sets; every step moves its own bytes.  The copies, events and the
-        decode entry point are called through ctypes with arguments marshalled
-        once, so the host keeps ahead of the GPU.  Returns (start, end) events
-        bracketing all copies and decodes."""
+        serving loop does, with two buffer sets.  The copy stream moves step
+        k + 1's inputs host -> device (one packed copy) while step k decodes on
+        the compute stream, then step k's `out` device -> host once it is done;
+        the next step's input copy is queued ahead of this step's output copy
+        so it never waits behind a decode.  Every step moves its own bytes.  The
+        copies, events and the decode entry point are called through ctypes
+        with arguments marshalled once, so the host keeps ahead of the GPU.
+        Returns (start, end) events bracketing all copies and decodes."""
         rt, lib = _cudart(), self.pa.load()
         cs, ks = self.copy_stream, self.compute_stream
         csh, ksh = ctypes.c_void_p(cs.cuda_stream), ctypes.c_void_p(ks.cuda_stream)
         if not hasattr(self, "_e2e_events"):
             evs = []
-            for _ in range(6):
+            for _ in range(4):
                 e = ctypes.c_void_p()
                 _rt_check(rt.cudaEventCreateWithFlags(ctypes.byref(e), 2))  # no timing
                 evs.append(e)
             self._e2e_events = evs
             self._e2e_args = [[self._decode_args(j, c, ksh) for c in range(self.copies)]
                               for j in range(2)]
-        h2d_ev, dec_ev, done_ev = self._e2e_events[0:2], self._e2e_events[2:4], self._e2e_events[4:6]
+        h2d_ev, dec_ev = self._e2e_events[0:2], self._e2e_events[2:4]
         entry = lib.pa_decode_mq if self.w.q_len > 1 else lib.pa_decode
         nbytes_in = host_in.numel()
         nbytes_out = self.e2e_out[0].numel() * self.e2e_out[0].element_size()
@@ -342,24 +343,33 @@ class Decoder:
         end = torch.cuda.Event(enable_timing=True)
         cs.wait_stream(torch.cuda.current_stream())
         ks.wait_stream(torch.cuda.current_stream())
-        start.record(cs)
-        for k in range(k0, k0 + n):
+
+        def h2d(k):
+            # Set k % 2 was last read by step k - 2, whose decode has ended.
             j = k % 2
             if k - k0 >= 2:
-                _rt_check(rt.cudaStreamWaitEvent(csh, done_ev[j], 0))
+                _rt_check(rt.cudaStreamWaitEvent(csh, dec_ev[j], 0))
             _rt_check(rt.cudaMemcpyAsync(ctypes.c_void_p(self.e2e_dev_in[j].data_ptr()),
                                          ctypes.c_void_p(host_in.data_ptr()), nbytes_in, 1, csh))
             _rt_check(rt.cudaEventRecord(h2d_ev[j], csh))
+
+        start.record(cs)
+        h2d(k0)
+        for k in range(k0, k0 + n):
+            j = k % 2
+            # Step k's inputs have landed; they were queued after step k - 2's
+            # output copy, so out[j] is free again as well.
             _rt_check(rt.cudaStreamWaitEvent(ksh, h2d_ev[j], 0))
             rc = entry(*self._e2e_args[j][k % self.copies])
             if rc != 0:
                 raise RuntimeError(f"decode returned {rc}")
             _rt_check(rt.cudaEventRecord(dec_ev[j], ksh))
+            if k + 1 < k0 + n:
+                h2d(k + 1)
             _rt_check(rt.cudaStreamWaitEvent(csh, dec_ev[j], 0))
             _rt_check(rt.cudaMemcpyAsync(ctypes.c_void_p(self.e2e_host_out[j].data_ptr()),
                                          ctypes.c_void_p(self.e2e_out[j].data_ptr()), nbytes_out, 2,
                                          csh))
-            _rt_check(rt.cudaEventRecord(done_ev[j], csh))
         cs.wait_stream(ks)
         end.record(cs)
         return start, end
@@ -518,7 +528,7 @@ def time_gpu(args, w: wl.Workload):
         },
         "e2e": {"value": round(world * dec.kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
-                "pipelined": "two buffer sets; step k's copies overlap step k +- 1's decode",
+                "pipelined": "two buffer sets; step k + 1's input copy and step k - 1's output copy overlap step k's decode",
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * dec.launches_per_step,
         "roofline": ({"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2),

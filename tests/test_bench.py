@@ -1,9 +1,12 @@
-"""bench.py's host logic on CPU: the kernel-source hash that voids a recorded
-ncu traffic figure, and the reference (oracle) arm's JSON line."""
+"""bench.py's host logic on CPU (the kernel-source hash that voids a recorded
+ncu traffic figure, the reference (oracle) arm's JSON line) and, on a GPU, its
+end-to-end loop's outputs."""
 import json
 import os
 import subprocess
 import sys
+
+import pytest
 
 from conftest import ROOT
 
@@ -53,3 +56,29 @@ def test_reference_arm_prints_one_json_line():
     assert d["higher_is_better"] is True and d["config"]["workload"] == "tiny"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.gpu
+def test_end_to_end_loop_returns_the_decode_output():
+    """bench.py's pipelined host-buffer loop: the outputs read back to host memory equal, bitwise,
+    a direct decode of the same step's inputs (the copies and the two buffer sets are ordered)."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import paged_kv_decode_v2_gb300 as pa
+    import workloads as wl
+    dec = bench.Decoder(wl.TINY, torch.device("cuda", 0))
+    host_in = dec.pack_host_inputs()
+    n = 5
+    dec.e2e_steps(0, n, host_in)
+    torch.cuda.synchronize()
+    inp, w = dec.inp, dec.w
+    S, H, D = inp.query.shape
+    tmp, es, ml = pa.alloc_workspace(S, H, D, max(1, dec.np), device="cuda")
+    for k in (n - 2, n - 1):
+        kc, vc = dec.caches[k % dec.copies]
+        ref = torch.empty_like(inp.query)
+        pa.pa_decode(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, w.partition_size,
+                     ref, tmp, es, ml, max_seq_len_hint=dec.max_seq_len)
+        torch.cuda.synchronize()
+        assert torch.equal(dec.e2e_host_out[k % 2], ref.cpu())
