@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
 
     __shared__ uint64_t bars[kMaxWarps * kMaxStages];
     __shared__ float s_factor[kMaxWarps][kMaxGroup];
-    __shared__ float s_stat[2][kMaxGroup]; // merged max, merged sum
+    __shared__ float s_stat[3][kMaxGroup]; // merged max, merged sum, 1 / sum (0 when empty)
     extern __shared__ uint8_t dyn_smem[];
 
     const int lane = threadIdx.x & 31;
@@ -474,27 +474,45 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
         }
         s_stat[0][h] = M;
         s_stat[1][h] = lsum;
+        // lsum == 0: no token of this range is visible to the column (only with
+        // several new tokens): an empty partition, or a zero output in V1.
+        s_stat[2][h] = lsum > 0.f ? 1.f / lsum : 0.f;
     }
     __syncthreads();
 
-    for (int idx = threadIdx.x; idx < ncols * D; idx += blockDim.x) {
-        const int h = idx / D;
-        const int d = idx % D;
-        float acc = 0.f;
-        for (int w = 0; w < nwarps; ++w)
-            acc = fmaf(s_factor[w][h], scr0[w * warp_stride + 2 * kHeads + h * kScr + d], acc);
-        const float lsum = s_stat[1][h];
-        // lsum == 0: no token of this range is visible to the column (only with
-        // several new tokens): an empty partition, or a zero output in V1.
-        const float val = lsum > 0.f ? acc / lsum : 0.f;
+    // Four consecutive dims per thread and pass (16-byte shared loads and a
+    // 16-byte partials store), the reciprocal of the sum taken once per head.
+    constexpr int kQuads = D / 4;
+    for (int idx = threadIdx.x; idx < ncols * kQuads; idx += blockDim.x) {
+        const int h = idx / kQuads;
+        const int d = (idx % kQuads) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int w = 0; w < nwarps; ++w) {
+            const float f = s_factor[w][h];
+            const float4 v =
+                *reinterpret_cast<const float4 *>(scr0 + w * warp_stride + 2 * kHeads + h * kScr + d);
+            acc.x = fmaf(f, v.x, acc.x);
+            acc.y = fmaf(f, v.y, acc.y);
+            acc.z = fmaf(f, v.z, acc.z);
+            acc.w = fmaf(f, v.w, acc.w);
+        }
+        const float inv = s_stat[2][h];
+        acc.x *= inv;
+        acc.y *= inv;
+        acc.z *= inv;
+        acc.w *= inv;
         const size_t bh = col_row(h);
         if (V1) {
-            static_cast<T *>(p.out)[bh * D + d] = E::from_float(val);
+            T *o4 = static_cast<T *>(p.out) + bh * D + d;
+            o4[0] = E::from_float(acc.x);
+            o4[1] = E::from_float(acc.y);
+            o4[2] = E::from_float(acc.z);
+            o4[3] = E::from_float(acc.w);
         } else {
             const size_t slot = bh * p.max_num_partitions + part;
-            p.tmp_output[slot * D + d] = val;
+            *reinterpret_cast<float4 *>(p.tmp_output + slot * D + d) = acc;
             if (d == 0) {
-                p.exp_sums[slot] = lsum;
+                p.exp_sums[slot] = s_stat[1][h];
                 p.max_logits[slot] = s_stat[0][h];
             }
         }
