@@ -26,8 +26,9 @@
 // S of tile t + 2 right behind P.V of tile t and the rows never wait for a
 // P.V before writing their next P.  The running max m used for P and for O
 // moves only when a row's max grows by more than 2^8 in exp2 terms (P then
-// stays <= 2^8, exactly representable scaling, no loss of precision); O is
-// rescaled, after waiting for the last P.V, only then.  O / l does not depend
+// stays <= 2^8, which fp32 and the 16-bit hi + lo pair hold with the same
+// relative precision as values <= 1); O is rescaled, after waiting for the
+// last P.V, only then.  O / l does not depend
 // on which m was used.  The true max is tracked beside it, and a V2 partial
 // reports that max with l rescaled to it, as the merge expects.
 //
