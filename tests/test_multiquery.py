@@ -137,3 +137,30 @@ def test_mq_bad_block_id_sets_status():
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
         run_mq(inp, 64, entry=e, status=st)
         assert int(st.item()) & 1
+
+
+def _random_mq_cases(n, seed):
+    """n seeded (q_len, G, D, bs, P, dtype, lens) draws over the shapes the entry points take."""
+    import random
+    rng = random.Random(seed)
+    cases = []
+    for k in range(n):
+        q_len = rng.choice([2, 3, 5, 8, 13, 16, 33, 64, 100, 200])
+        G = rng.choice([1, 2, 4, 8, 16])
+        D = rng.choice([64, 128, 128, 256])
+        bs = rng.choice([8, 16, 16, 32, 64])
+        P = rng.choice([bs, 4 * bs, 512, rng.randint(1, 700)])
+        dtype = rng.choice([wl.F16, wl.BF16])
+        S = rng.randint(1, 4)
+        lens = tuple(rng.choice([0, 1, rng.randint(1, q_len + 2), rng.randint(1, 1500)]) for _ in range(S))
+        cases.append((q_len, G, D, bs, P, dtype, lens, 7000 + k))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_mq_cases(32, 20261203), ids=lambda c: f"q{c[0]}g{c[1]}d{c[2]}b{c[3]}p{c[4]}")
+def test_mq_random_shapes_default_dispatch(case):
+    """Seeded random shapes through the default kernel choice (mma.sync below 64 rows per KV head,
+    a tcgen05 kernel from 64), V1 and V2, element by element against the oracle."""
+    q_len, G, D, bs, P, dtype, lens, seed = case
+    w = mq("mq_random", q_len, G, lens, bs=bs, P=P, D=D, dtype=dtype, seed=seed)
+    check_mq(wl.make_inputs(w, device="cuda"), P)
