@@ -112,10 +112,14 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     const int ntiles = tokE > tokA ? (tokE - tok0 + kTcTok - 1) / kTcTok : 0;
     const int nblk = tokE > tokA ? (tokE - tok0 + BS - 1) / BS : 0;
 
-    // This thread's row (warps 0-3).
+    // This thread's row (warps 0-3).  A tile of fewer than 128 rows puts them
+    // in the highest warps (M index = roff + row): whole warps of padding rows
+    // then sit on the schedulers of the MMA and TMA warps and skip the
+    // softmax, while the rows run on schedulers of their own.
+    const int roff = kTcRows - (nrows + 31) / 32 * 32;
     const int r = threadIdx.x;
-    const bool row_ok = r < kTcRows && r < nrows;
-    const int ci = c0 + (row_ok ? r : 0);
+    const bool row_ok = r < kTcRows && r >= roff && r - roff < nrows;
+    const int ci = c0 + (row_ok ? r - roff : 0);
     const int qi = ci / p.group;                 // new token
     const int head = kv * p.group + ci % p.group;
     const size_t qrow = ((size_t)b * p.q_len + qi) * p.num_heads + head;
@@ -367,194 +371,209 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             fence_proxy_async();
             mbar_arrive(b_q_full);
         }
-        // Visible tokens of this row: tokA <= t < hi (unsigned span from tokA).
-        const int hi = row_ok ? min(tokE, L - p.q_len + qi + 1) : tokA;
-        const unsigned span = (unsigned)max(hi - tokA, 0);
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-        const float scale = p.scale;
-        // m_run: the max P and O are relative to; m_true: the row's max.
-        float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
-        bool ok = true;
-        for (int t = 0; t < ntiles; ++t) {
-            const uint32_t sc = lane_base + C::kSCol + (uint32_t)(t & 1) * kTcTok;
-            // Waits end in a warp-uniform decision: tcgen05.ld / st are warp-collective.
-            if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full + 8 * (t & 1),
-                                                             (uint32_t)(t >> 1) & 1u, abort_flag))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            uint32_t sr[2][32];
-            tmem_ld32_async(sc, sr[0]);
-            tmem_ld32_async(sc + 32, sr[1]);
-            tmem_ld_wait(sr[0]);
-            tmem_ld_wait(sr[1]);
-
-            const int off = tok0 + t * kTcTok - tokA; // token (t's first) - tokA
-            // x: the exp2 argument is x * cf - mb.  On a tile every row of the
-            // warp sees whole (the common case) with scale > 0, x is the raw
-            // score and the scale folds into cf (max(s) * scale = max(s * scale)
-            // for scale > 0); otherwise x = s * scale, or -inf where masked.
-            float x[kTcTok];
-            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}; // independent chains
-            float mx, cf;
-            if (__all_sync(0xffffffffu, scale > 0.f && off >= 0 && off + kTcTok <= (int)span)) {
-#pragma unroll
-                for (int c = 0; c < kTcTok; ++c) {
-                    x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+        if (warp * 32 + 32 <= roff) {
+            // A warp of padding rows only: one arrival on "P ready" per tile,
+            // after that tile's S, keeps the barrier's count (never a phase
+            // early); its P lanes are never read into a row that is stored.
+            for (int t = 0; t < ntiles; ++t) {
+                if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full + 8 * (t & 1),
+                                                                 (uint32_t)(t >> 1) & 1u, abort_flag))) {
+                    status_bits |= PA_STATUS_TIMEOUT;
+                    *abort_flag = 1;
+                    break;
                 }
-                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale;
-                cf = scale * kLog2e;
-            } else {
-#pragma unroll
-                for (int c = 0; c < kTcTok; ++c) {
-                    const float s = __uint_as_float(sr[c >> 5][c & 31]);
-                    x[c] = (unsigned)(off + c) < span ? s * scale : -INFINITY;
-                    mq[c & 3] = fmaxf(mq[c & 3], x[c]);
-                }
-                mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-                cf = kLog2e;
+                mbar_arrive(b_p_full + 8 * (t & 1));
             }
-            m_true = fmaxf(m_true, mx);
-            // Move m when a row of the warp would otherwise see P > 2^8 (the
-            // first visible tile always: m_run = -inf).  NaN (both -inf) is no.
-            float a = 1.f;
-            if (__any_sync(0xffffffffu, (mx - m_run) * kLog2e > kTcRescaleLog2)) {
-                const float mn = fmaxf(m_run, mx);
-                // A row with no visible token yet (max still -inf) keeps l = o = 0.
-                a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
-                m_run = mn;
-                // O is rescaled once the last P.V has landed (tile 0 has no O yet).
-                if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
-                                                        (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int cc = 0; cc < D; cc += 64) {
-                        uint32_t o0[32], o1[32];
-                        tmem_ld32_async(lane_base + cc, o0);
-                        tmem_ld32_async(lane_base + cc + 32, o1);
-                        tmem_ld_wait(o0);
-                        tmem_ld_wait(o1);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            o0[k] = __float_as_uint(__uint_as_float(o0[k]) * a);
-                            o1[k] = __float_as_uint(__uint_as_float(o1[k]) * a);
-                        }
-                        tmem_st32x2(lane_base + cc, o0, lane_base + cc + 32, o1);
-                    }
-                }
-            }
-            const float mb = m_run != -INFINITY ? m_run * kLog2e : 0.f;
-            uint32_t ph[32], pl[32];
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < kTcTok; c += 2) {
-                const float p0 = fast_exp2(fmaf(x[c], cf, -mb));
-                const float p1 = fast_exp2(fmaf(x[c + 1], cf, -mb));
-                ls[(c >> 1) & 3] += p0 + p1;
-                const uint32_t h = E::pack(p0, p1);
-                ph[c >> 1] = h;
-                pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
-            }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l_run = fmaf(l_run, a, lsum);
-
-            // P over S in the same buffer: its S was read above, and P.V(t - 2),
-            // the last reader of the buffer, completed before S(t) did.
-            if (kBf16)
-                tmem_st32x2(sc, ph, sc + 32, pl);
-            else
-                tmem_st32(sc, ph);
-
-            if (t == ntiles - 1) {
-                // Tile rows past the range (unloaded blocks, slots past the
-                // sequence end) may hold anything: zero them in V so that
-                // 0 * garbage cannot reach O.
-                const int vt = tokE - (tok0 + t * kTcTok);
-                if (vt < kTcTok) {
-                    const int s = t % vst;
-                    // The parity wait for V(t) is unambiguous once the stage's
-                    // previous fill, V(t - vst), has landed.  S(t) followed
-                    // P.V(t - 2), so that holds for vst >= 2; a one-stage ring
-                    // waits for P.V(t - 1) first.
-                    if (vst == 1 && t > 0 &&
-                        !__all_sync(0xffffffffu,
-                                    mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
-                                                        (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
-                        ok = false;
-                        break;
-                    }
-                    if (!__all_sync(0xffffffffu,
-                                    mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u,
-                                                        abort_flag))) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t vb = v_sm + (uint32_t)s * C::kKVBytes;
-                    const int nchunks = (kTcTok - vt) * 8 * C::kSlices;
-                    for (int idx = r; idx < nchunks; idx += kTcRows) {
-                        const int sl = idx % C::kSlices;
-                        const int rest = idx / C::kSlices;
-                        st_shared_zero16(vb + sl * C::kKVSlice + (vt + rest / 8) * 128 + (rest & 7) * 16);
-                    }
-                    fence_proxy_async();
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(b_p_full + 8 * (t & 1));
-        }
-        // P.V(ntiles - 1), the last MMA; P.V(ntiles - 3) completed before
-        // S(ntiles - 1), so the parity wait cannot be a phase early.
-        if (ok && !__all_sync(0xffffffffu,
-                              mbar_wait_abortable(b_o_done + 8 * ((ntiles - 1) & 1),
-                                                  (uint32_t)((ntiles - 1) >> 1) & 1u, abort_flag)))
-            ok = false;
-        if (!ok) {
-            status_bits |= PA_STATUS_TIMEOUT;
-            *abort_flag = 1;
         } else {
-            tc_fence_after();
-            // ---- epilogue: O / l for the row
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            if (V1) {
-                uint32_t *out = reinterpret_cast<uint32_t *>(static_cast<T *>(p.out) + qrow * D);
-#pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + cc, o);
-                    if (row_ok) {
+            // Visible tokens of this row: tokA <= t < hi (unsigned span from tokA).
+            const int hi = row_ok ? min(tokE, L - p.q_len + qi + 1) : tokA;
+            const unsigned span = (unsigned)max(hi - tokA, 0);
+            const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+            const float scale = p.scale;
+            // m_run: the max P and O are relative to; m_true: the row's max.
+            float m_run = -INFINITY, m_true = -INFINITY, l_run = 0.f;
+            bool ok = true;
+            for (int t = 0; t < ntiles; ++t) {
+                const uint32_t sc = lane_base + C::kSCol + (uint32_t)(t & 1) * kTcTok;
+                // Waits end in a warp-uniform decision: tcgen05.ld / st are warp-collective.
+                if (!__all_sync(0xffffffffu, mbar_wait_abortable(b_s_full + 8 * (t & 1),
+                                                                 (uint32_t)(t >> 1) & 1u, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t sr[2][32];
+                tmem_ld32_async(sc, sr[0]);
+                tmem_ld32_async(sc + 32, sr[1]);
+                tmem_ld_wait(sr[0]);
+                tmem_ld_wait(sr[1]);
+
+                const int off = tok0 + t * kTcTok - tokA; // token (t's first) - tokA
+                // x: the exp2 argument is x * cf - mb.  On a tile every row of the
+                // warp sees whole (the common case) with scale > 0, x is the raw
+                // score and the scale folds into cf (max(s) * scale = max(s * scale)
+                // for scale > 0); otherwise x = s * scale, or -inf where masked.
+                float x[kTcTok];
+                float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}; // independent chains
+                float mx, cf;
+                if (__all_sync(0xffffffffu, scale > 0.f && off >= 0 && off + kTcTok <= (int)span)) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2)
-                            out[(cc + k) / 2] = E::pack(__uint_as_float(o[k]) * inv,
-                                                        __uint_as_float(o[k + 1]) * inv);
+                    for (int c = 0; c < kTcTok; ++c) {
+                        x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                        mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                    }
+                    mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * scale;
+                    cf = scale * kLog2e;
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kTcTok; ++c) {
+                        const float s = __uint_as_float(sr[c >> 5][c & 31]);
+                        x[c] = (unsigned)(off + c) < span ? s * scale : -INFINITY;
+                        mq[c & 3] = fmaxf(mq[c & 3], x[c]);
+                    }
+                    mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+                    cf = kLog2e;
+                }
+                m_true = fmaxf(m_true, mx);
+                // Move m when a row of the warp would otherwise see P > 2^8 (the
+                // first visible tile always: m_run = -inf).  NaN (both -inf) is no.
+                float a = 1.f;
+                if (__any_sync(0xffffffffu, (mx - m_run) * kLog2e > kTcRescaleLog2)) {
+                    const float mn = fmaxf(m_run, mx);
+                    // A row with no visible token yet (max still -inf) keeps l = o = 0.
+                    a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
+                    m_run = mn;
+                    // O is rescaled once the last P.V has landed (tile 0 has no O yet).
+                    if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
+                                                            (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < D; cc += 64) {
+                            uint32_t o0[32], o1[32];
+                            tmem_ld32_async(lane_base + cc, o0);
+                            tmem_ld32_async(lane_base + cc + 32, o1);
+                            tmem_ld_wait(o0);
+                            tmem_ld_wait(o1);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) {
+                                o0[k] = __float_as_uint(__uint_as_float(o0[k]) * a);
+                                o1[k] = __float_as_uint(__uint_as_float(o1[k]) * a);
+                            }
+                            tmem_st32x2(lane_base + cc, o0, lane_base + cc + 32, o1);
+                        }
                     }
                 }
+                const float mb = m_run != -INFINITY ? m_run * kLog2e : 0.f;
+                uint32_t ph[32], pl[32];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < kTcTok; c += 2) {
+                    const float p0 = fast_exp2(fmaf(x[c], cf, -mb));
+                    const float p1 = fast_exp2(fmaf(x[c + 1], cf, -mb));
+                    ls[(c >> 1) & 3] += p0 + p1;
+                    const uint32_t h = E::pack(p0, p1);
+                    ph[c >> 1] = h;
+                    pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(h), p1 - E::hi(h)) : 0u;
+                }
+                const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                l_run = fmaf(l_run, a, lsum);
+
+                // P over S in the same buffer: its S was read above, and P.V(t - 2),
+                // the last reader of the buffer, completed before S(t) did.
+                if (kBf16)
+                    tmem_st32x2(sc, ph, sc + 32, pl);
+                else
+                    tmem_st32(sc, ph);
+
+                if (t == ntiles - 1) {
+                    // Tile rows past the range (unloaded blocks, slots past the
+                    // sequence end) may hold anything: zero them in V so that
+                    // 0 * garbage cannot reach O.
+                    const int vt = tokE - (tok0 + t * kTcTok);
+                    if (vt < kTcTok) {
+                        const int s = t % vst;
+                        // The parity wait for V(t) is unambiguous once the stage's
+                        // previous fill, V(t - vst), has landed.  S(t) followed
+                        // P.V(t - 2), so that holds for vst >= 2; a one-stage ring
+                        // waits for P.V(t - 1) first.
+                        if (vst == 1 && t > 0 &&
+                            !__all_sync(0xffffffffu,
+                                        mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
+                                                            (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        if (!__all_sync(0xffffffffu,
+                                        mbar_wait_abortable(b_v_full + 8 * s, (uint32_t)(t / vst) & 1u,
+                                                            abort_flag))) {
+                            ok = false;
+                            break;
+                        }
+                        const uint32_t vb = v_sm + (uint32_t)s * C::kKVBytes;
+                        const int nchunks = (kTcTok - vt) * 8 * C::kSlices;
+                        for (int idx = r - roff; idx < nchunks; idx += kTcRows - roff) {
+                            const int sl = idx % C::kSlices;
+                            const int rest = idx / C::kSlices;
+                            st_shared_zero16(vb + sl * C::kKVSlice + (vt + rest / 8) * 128 + (rest & 7) * 16);
+                        }
+                        fence_proxy_async();
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(b_p_full + 8 * (t & 1));
+            }
+            // P.V(ntiles - 1), the last MMA; P.V(ntiles - 3) completed before
+            // S(ntiles - 1), so the parity wait cannot be a phase early.
+            if (ok && !__all_sync(0xffffffffu,
+                                  mbar_wait_abortable(b_o_done + 8 * ((ntiles - 1) & 1),
+                                                      (uint32_t)((ntiles - 1) >> 1) & 1u, abort_flag)))
+                ok = false;
+            if (!ok) {
+                status_bits |= PA_STATUS_TIMEOUT;
+                *abort_flag = 1;
             } else {
-                const size_t slot = qrow * p.max_num_partitions + part;
-                float4 *tmp = reinterpret_cast<float4 *>(p.tmp_output + slot * D);
+                tc_fence_after();
+                // ---- epilogue: O / l for the row
+                const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+                if (V1) {
+                    uint32_t *out = reinterpret_cast<uint32_t *>(static_cast<T *>(p.out) + qrow * D);
 #pragma unroll 1
-                for (int cc = 0; cc < D; cc += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + cc, o);
-                    if (row_ok) {
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + cc, o);
+                        if (row_ok) {
 #pragma unroll
-                        for (int k = 0; k < 32; k += 4)
-                            tmp[(cc + k) / 4] = make_float4(
-                                __uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
-                                __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                            for (int k = 0; k < 32; k += 2)
+                                out[(cc + k) / 2] = E::pack(__uint_as_float(o[k]) * inv,
+                                                            __uint_as_float(o[k + 1]) * inv);
+                        }
                     }
-                }
-                if (row_ok) {
-                    // The partition's statistics relative to its true max.
-                    p.exp_sums[slot] =
-                        m_true != -INFINITY ? l_run * fast_exp2((m_run - m_true) * kLog2e) : 0.f;
-                    p.max_logits[slot] = m_true;
+                } else {
+                    const size_t slot = qrow * p.max_num_partitions + part;
+                    float4 *tmp = reinterpret_cast<float4 *>(p.tmp_output + slot * D);
+#pragma unroll 1
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(lane_base + cc, o);
+                        if (row_ok) {
+#pragma unroll
+                            for (int k = 0; k < 32; k += 4)
+                                tmp[(cc + k) / 4] = make_float4(
+                                    __uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                                    __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+                        }
+                    }
+                    if (row_ok) {
+                        // The partition's statistics relative to its true max.
+                        p.exp_sums[slot] =
+                            m_true != -INFINITY ? l_run * fast_exp2((m_run - m_true) * kLog2e) : 0.f;
+                        p.max_logits[slot] = m_true;
+                    }
                 }
             }
         }
