@@ -51,7 +51,7 @@ KERNEL_SOURCES = {
               "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
 }
 # From this many query rows per KV head the library runs the tcgen05 kernel.
-TC_MIN_ROWS = 64
+TC_MIN_ROWS = 32
 
 
 # ---------------------------------------------------------------- distributed plumbing

@@ -185,8 +185,8 @@ PA_API int pa_decode_v2_phase2(const int32_t *seq_lens, int num_seqs, int num_he
  * A partition holding none of the tokens a query sees is written as
  * max_logits = -inf, exp_sums = 0, tmp_output = 0 and adds nothing to the
  * merge.  The K/V cache is read once per call for all q_len * G query rows
- * of a KV head: up to 63 rows an mma.sync kernel serves 16 rows per CTA,
- * from 64 rows a tcgen05 kernel serves 128 rows per CTA (see
+ * of a KV head: up to 31 rows an mma.sync kernel serves 16 rows per CTA,
+ * from 32 rows a tcgen05 kernel serves 128 rows per CTA (see
  * pa_set_rows_kernel); CTAs that split the rows of one range run side by
  * side, so their reads meet in L2.  Chunked prefill is this call with q_len
  * the chunk length, the chunk's own K/V already written to the cache (it
@@ -214,7 +214,7 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
  * Host only.  V1 when one partition covers max_seq_len, or when the V1 grid
  * (num_seqs * num_kv_heads CTAs for every CTA that splits a KV head's
  * q_len * G query rows) gives every SM at least one CTA and a KV head has
- * at least 16 query rows; otherwise V2.  There is no counterpart in the
+ * at least 32 query rows (the tcgen05 kernel's); otherwise V2.  There is no counterpart in the
  * method's description, which dispatches single-token decode only.
  */
 PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
@@ -274,8 +274,8 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
 
 /*
  * Kernel choice for the query rows of a KV head (rows = q_len * G),
- * process-wide: 0 (default) picks by row count -- up to 63 rows the
- * mma.sync kernel (16 rows per CTA), from 64 rows a tcgen05 kernel (128-row
+ * process-wide: 0 (default) picks by row count -- up to 31 rows the
+ * mma.sync kernel (16 rows per CTA), from 32 rows a tcgen05 kernel (128-row
  * query tiles, S and O accumulated in tensor memory; two tiles sharing each
  * K/V tile per CTA for fp16 when a KV head has more than 128 rows, head_dim
  * <= 128 and sequences reach 1024 tokens, else one tile and two CTAs per

@@ -24,7 +24,10 @@ std::atomic<int> g_tune_stages{0};
 std::atomic<int> g_rows_kernel{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
-constexpr int kTcMinRows = 64;
+// Measured on GB300 (best of V1 / V2 per kernel, mma.sync vs tcgen05):
+// 16 rows 99 vs 155 us; 32 rows: batch decode 152 vs 151, fp16 138 vs 140,
+// a 100K-token sequence 64.5 vs 54.8; 48 rows 211 vs 161; 64 rows 291 vs 157.
+constexpr int kTcMinRows = 32;
 
 // Per-device cached multiprocessor count (0 = not queried yet).
 std::atomic<int> g_sm_count[kMaxDevices];
@@ -552,14 +555,15 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 }
 
 // Several new tokens per sequence: V1 when one partition covers the
-// sequences, or when its grid (num_seqs * num_kv_heads CTAs per row split)
-// already gives every SM a CTA and a KV head has at least 16 query rows, so
-// each CTA carries enough work; otherwise V2.  Measured on GB300, batch
-// decode (32 seqs up to 8192 tokens, 32 / 8 heads) checking q_len tokens:
-// q_len 2: V2 92 vs V1 100 us; 4: V1 113 vs 123; 8: V1 157 vs 223; 16: V1
-// 178 vs 188; 32: V1 173 vs 235; 100K-token sequence, q_len 16: V2 87 vs V1
-// 1615 us; chunked prefill (2 x 2048 new tokens after 30K): V1 2384 vs V2
-// 4867 us.
+// sequences, or when a KV head's query rows go to the tcgen05 kernel and
+// its V1 grid (num_seqs * num_kv_heads CTAs per row split) already gives
+// every SM a CTA, so each CTA carries enough work; otherwise V2.  Measured
+// on GB300, batch decode (32 seqs up to 8192 tokens, 32 / 8 heads)
+// checking q_len tokens: q_len 2 (mma.sync): V2 92 vs V1 100 us; 4
+// (mma.sync): V2 99 vs V1 109; 8 (tcgen05): V1 151 vs V2 152; 12: V1 161
+// vs 175; 16: V1 157 vs 173; 32: V1 174 vs 235; 100K-token sequence, q_len
+// 16: V2 87 vs V1 1615 us; chunked prefill (2 x 2048 new tokens after 30K):
+// V1 2384 vs V2 4867 us.
 int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int head_dim,
                       int max_seq_len, int partition_size, int sms)
 {
@@ -570,7 +574,7 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
     // tiles, which happens only for many-row steps that fill the GPU anyway).
     const long long ctas =
         (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim, PA_BF16, max_seq_len);
-    return (cols >= 16 && ctas >= sms) ? 1 : 2;
+    return (cols >= kTcMinRows && ctas >= sms) ? 1 : 2;
 }
 
 } // namespace

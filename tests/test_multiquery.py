@@ -67,7 +67,8 @@ def test_mq_dispatch_rule_and_entry(cuda_lib):
     import paged_kv_decode_v2_gb300 as pa
     # batch decode shapes (32 seqs, 32 / 8 heads, up to 8192 tokens, P = 512)
     assert pa.pa_decode_mq_choose(32, 2, 32, 8, 128, 8192, 512) == 2   # 8 rows per KV head
-    assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 8192, 512) == 1   # 16 rows, 256 CTAs
+    assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 8192, 512) == 2   # 16 rows (mma.sync)
+    assert pa.pa_decode_mq_choose(32, 8, 32, 8, 128, 8192, 512) == 1   # 32 rows (tcgen05), 256 CTAs
     assert pa.pa_decode_mq_choose(32, 32, 32, 8, 128, 8192, 512) == 1
     assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 100000, 512) == 2  # one long sequence
     assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 512, 512) == 1     # one partition
@@ -159,8 +160,8 @@ def _random_mq_cases(n, seed):
 
 @pytest.mark.parametrize("case", _random_mq_cases(32, 20261203), ids=lambda c: f"q{c[0]}g{c[1]}d{c[2]}b{c[3]}p{c[4]}")
 def test_mq_random_shapes_default_dispatch(case):
-    """Seeded random shapes through the default kernel choice (mma.sync below 64 rows per KV head,
-    a tcgen05 kernel from 64), V1 and V2, element by element against the oracle."""
+    """Seeded random shapes through the default kernel choice (mma.sync below 32 rows per KV head,
+    a tcgen05 kernel from 32), V1 and V2, element by element against the oracle."""
     q_len, G, D, bs, P, dtype, lens, seed = case
     w = mq("mq_random", q_len, G, lens, bs=bs, P=P, D=D, dtype=dtype, seed=seed)
     check_mq(wl.make_inputs(w, device="cuda"), P)
