@@ -47,10 +47,12 @@ def check_single(inp, P):
             check_partitions(inp, P, tmp, es, ml, prob=prob)
 
 
-@pytest.mark.parametrize("q_len,G", [(2, 16), (4, 8), (8, 4), (3, 16), (32, 4), (16, 8), (33, 4)])
+@pytest.mark.parametrize("q_len,G", [(2, 16), (4, 8), (8, 4), (3, 16), (5, 4), (20, 4), (24, 4),
+                                     (32, 4), (16, 8), (33, 4)])
 @pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
 def test_tc_row_counts(q_len, G, dtype):
-    """32 to 132 rows per KV head: padding rows, exactly one CTA, two CTAs."""
+    """20 to 132 rows per KV head: a tile's rows in one, two, three or four warps (whole warps of
+    padding rows idle), exactly one CTA, two CTAs."""
     P = 128
     lens = (1, q_len, 63, 64, 65, P - 1, P + 1, 2 * P + 70, 700)
     w = mq("tc_rows", q_len, G, lens, P=P, dtype=dtype, seed=8000 + 31 * q_len + G + dtype)
