@@ -516,7 +516,7 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
     const int qrc = check_q_len(num_seqs, q_len);
     if (qrc)
         return qrc;
-    if (!aligned(tmp_output, 16) || !aligned(out, 2))
+    if (!aligned(tmp_output, 16) || !aligned(out, 4))
         return PA_ERR_INVALID_ARG;
     if (pa_v2_num_partitions(max_seq_len, partition_size) > max_num_partitions)
         return PA_ERR_WORKSPACE;
@@ -630,7 +630,7 @@ PA_API int pa_decode_v2_mq(const void *query, const void *key_cache, const void 
                            void *out, float *tmp_output, float *exp_sums, float *max_logits,
                            int max_num_partitions, int32_t *status, pa_stream_t stream)
 {
-    if (!out || !aligned(out, 2))
+    if (!out || !aligned(out, 4))
         return PA_ERR_INVALID_ARG;
     int cap = 0;
     int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
@@ -674,7 +674,7 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
     rc = check_q_len(num_seqs, q_len);
     if (rc)
         return rc;
-    if (!out || !aligned(out, 2))
+    if (!out || !aligned(out, 4))
         return PA_ERR_INVALID_ARG;
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     AttnLaunch L;

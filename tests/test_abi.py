@@ -85,6 +85,8 @@ def _v2(lib, **kw):
     (dict(partition_size=-16), 1),
     (dict(partition_size=0), 1),
     (dict(key_cache=FAKE + 8), 1),
+    (dict(query=FAKE + 2), 1),
+    (dict(out=FAKE + 2), 1),
     (dict(max_np=1), 3),
     (dict(hint=600, max_np=1), 3),
 ])
@@ -98,6 +100,7 @@ def test_invalid_arguments_v1_and_dispatch(cuda_lib):
     assert lib.pa_decode_v1(*args, 0, FAKE, None, None) == 2
     args = [FAKE] * 5 + [1, 8, 2, 128, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_v1(*args, 0, None, None, None) == 1
+    assert lib.pa_decode_v1(*args, 0, FAKE + 2, None, None) == 1   # out must be 4-byte aligned
     assert lib.pa_decode(*args, -500, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
     assert lib.pa_decode_v2_phase2(FAKE, 1, 8, 128, 1000, 512, 0, FAKE, FAKE, FAKE, 1, FAKE,
                                    None, None) == 3
