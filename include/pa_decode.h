@@ -54,8 +54,9 @@
  * num_kv_heads an integer in [1, 64]; q_len in [1, 4096] with num_seqs *
  * q_len <= 65535 (the _mq entry points).  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned
- * (they are read with the Tensor Memory Accelerator); query and out 4-byte
- * aligned.
+ * (they are read with the Tensor Memory Accelerator), tmp_output 16-byte
+ * aligned, and query, out, block_tables, seq_lens, exp_sums and max_logits
+ * 4-byte aligned; a misaligned pointer is PA_ERR_INVALID_ARG.
  *
  * Ownership, synchronisation, errors
  * ----------------------------------

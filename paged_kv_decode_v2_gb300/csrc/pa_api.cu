@@ -96,7 +96,8 @@ int check_shape(const void *query, const void *key_cache, const void *value_cach
     if ((int64_t)num_blocks * num_kv_heads * block_size > INT32_MAX ||
         (int64_t)max_blocks_per_seq * block_size > INT32_MAX)
         return PA_ERR_UNSUPPORTED;
-    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(query, 4))
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16) || !aligned(query, 4) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PA_ERR_INVALID_ARG;
     return PA_OK;
 }
@@ -516,7 +517,8 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
     const int qrc = check_q_len(num_seqs, q_len);
     if (qrc)
         return qrc;
-    if (!aligned(tmp_output, 16) || !aligned(out, 4))
+    if (!aligned(tmp_output, 16) || !aligned(out, 4) || !aligned(seq_lens, 4) ||
+        !aligned(exp_sums, 4) || !aligned(max_logits, 4))
         return PA_ERR_INVALID_ARG;
     if (pa_v2_num_partitions(max_seq_len, partition_size) > max_num_partitions)
         return PA_ERR_WORKSPACE;

@@ -87,6 +87,8 @@ def _v2(lib, **kw):
     (dict(key_cache=FAKE + 8), 1),
     (dict(query=FAKE + 2), 1),
     (dict(out=FAKE + 2), 1),
+    (dict(block_tables=FAKE + 2), 1),
+    (dict(seq_lens=FAKE + 1), 1),
     (dict(max_np=1), 3),
     (dict(hint=600, max_np=1), 3),
 ])
