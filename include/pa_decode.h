@@ -55,8 +55,8 @@
  * q_len <= 65535 (the _mq entry points).  Other shapes return
  * PA_ERR_UNSUPPORTED.  key_cache and value_cache must be 16-byte aligned
  * (they are read with the Tensor Memory Accelerator), tmp_output 16-byte
- * aligned, and query, out, block_tables, seq_lens, exp_sums and max_logits
- * 4-byte aligned; a misaligned pointer is PA_ERR_INVALID_ARG.
+ * aligned, and query, out, block_tables, seq_lens, exp_sums, max_logits and
+ * status 4-byte aligned; a misaligned pointer is PA_ERR_INVALID_ARG.
  *
  * Ownership, synchronisation, errors
  * ----------------------------------

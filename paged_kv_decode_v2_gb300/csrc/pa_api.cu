@@ -478,7 +478,8 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
         return PA_ERR_INVALID_ARG;
     if (!tmp_output || !exp_sums || !max_logits || max_num_partitions <= 0)
         return PA_ERR_INVALID_ARG;
-    if (!aligned(tmp_output, 16) || !aligned(exp_sums, 4) || !aligned(max_logits, 4))
+    if (!aligned(tmp_output, 16) || !aligned(exp_sums, 4) || !aligned(max_logits, 4) ||
+        (status && !aligned(status, 4)))
         return PA_ERR_INVALID_ARG;
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     const int np = pa_v2_num_partitions(cap, partition_size);
@@ -518,7 +519,7 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
     if (qrc)
         return qrc;
     if (!aligned(tmp_output, 16) || !aligned(out, 4) || !aligned(seq_lens, 4) ||
-        !aligned(exp_sums, 4) || !aligned(max_logits, 4))
+        !aligned(exp_sums, 4) || !aligned(max_logits, 4) || (status && !aligned(status, 4)))
         return PA_ERR_INVALID_ARG;
     if (pa_v2_num_partitions(max_seq_len, partition_size) > max_num_partitions)
         return PA_ERR_WORKSPACE;
@@ -676,7 +677,7 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
     rc = check_q_len(num_seqs, q_len);
     if (rc)
         return rc;
-    if (!out || !aligned(out, 4))
+    if (!out || !aligned(out, 4) || (status && !aligned(status, 4)))
         return PA_ERR_INVALID_ARG;
     const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
     AttnLaunch L;
@@ -824,7 +825,7 @@ PA_API int pa_set_rows_kernel(int mode)
 
 PA_API int pa_selftest_wait_timeout(int32_t *status, long long limit_ns, pa_stream_t stream)
 {
-    if (!status || limit_ns <= 0 || limit_ns > 2000000000LL)
+    if (!status || !aligned(status, 4) || limit_ns <= 0 || limit_ns > 2000000000LL)
         return PA_ERR_INVALID_ARG;
     return launch_wait_selftest(status, (unsigned long long)limit_ns, (cudaStream_t)stream) ==
                    cudaSuccess

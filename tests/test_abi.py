@@ -89,6 +89,7 @@ def _v2(lib, **kw):
     (dict(out=FAKE + 2), 1),
     (dict(block_tables=FAKE + 2), 1),
     (dict(seq_lens=FAKE + 1), 1),
+    (dict(status=FAKE + 2), 1),
     (dict(max_np=1), 3),
     (dict(hint=600, max_np=1), 3),
 ])
@@ -141,6 +142,7 @@ def test_rows_kernel_override_validation(cuda_lib):
 def test_selftest_rejects_bad_limits(cuda_lib):
     lib = cuda_lib.load()
     assert lib.pa_selftest_wait_timeout(None, 1000, None) == 1
+    assert lib.pa_selftest_wait_timeout(FAKE + 2, 1000, None) == 1
     assert lib.pa_selftest_wait_timeout(FAKE, 0, None) == 1
     assert lib.pa_selftest_wait_timeout(FAKE, 3_000_000_000, None) == 1
 
