@@ -532,7 +532,9 @@ def time_gpu(args, w: wl.Workload):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * dec.launches_per_step,
         "roofline": ({"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2),
-                      "peak": tpeak, "peak_kind": tpeak_kind + " dense bf16 (burst)",
+                      "peak": tpeak,
+                      "peak_kind": tpeak_kind + (" dense bf16 (burst)" if w.dtype == wl.BF16 else
+                                                 " dense bf16 (burst) x 1, fp16's nominal ratio"),
                       "unit": "TFLOP/s", "frac": round(k1_tflops / tpeak, 4)}
                      if tensor_bound else
                      {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2),

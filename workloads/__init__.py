@@ -88,9 +88,11 @@ SPEC_VERIFY16 = BATCH.with_(name="spec_verify_16", q_len=16)
 # to the cache) after a 30,720-token prefix; 32 query / 8 KV heads.
 CHUNKED_PREFILL = Workload("chunked_prefill", 2, 32, 8, 128, 16, 512, BF16, "fixed",
                            seq_len=32768, q_len=2048, seed=20261207)
+# The same step with fp16 storage (run by the two-query-tile kernel).
+CHUNKED_PREFILL_F16 = CHUNKED_PREFILL.with_(name="chunked_prefill_f16", dtype=F16)
 
 ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS, BATCH_SPEC4,
-                           SPEC_VERIFY16, CHUNKED_PREFILL)}
+                           SPEC_VERIFY16, CHUNKED_PREFILL, CHUNKED_PREFILL_F16)}
 
 
 def draw_seq_lens(w: Workload) -> list:
