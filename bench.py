@@ -40,6 +40,12 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 METRIC = "paged-decode attention effective KV-read GB/s (% of HBM peak); µs per call"
 DEFAULT_CONFIG = "batch_decode"
+# Timed after the headline in the same run: the 100K-token decode at both
+# partition sizes and the largest workload (4.3 GB of K/V).
+PER_CONFIG = ("long_100k", "long_100k_p1024", "stress")
+# The HBM3e figure quoted for the part (about 8 TB/s); the measured copy
+# bandwidth is the roofline's denominator, this one is reported beside it.
+NOMINAL_HBM_GBS = 8000.0
 # Sources of each kernel family, hashed to void a recorded ncu traffic figure
 # once the kernel changes.
 KERNEL_SOURCES = {
@@ -218,6 +224,7 @@ class Decoder:
             v = torch.randn(base.value_cache.shape, generator=g, device=device).to(base.value_cache.dtype)
             self.caches.append((k, v))
         self.inp = base
+        self.sum_seq_len = int(base.seq_lens.sum().item())
         S, H, D = base.query.shape[0], w.num_heads, w.head_dim
         self.cap = base.block_tables.shape[1] * w.block_size
         self.max_seq_len = base.max_seq_len
@@ -245,6 +252,13 @@ class Decoder:
         self.flops = 4 * w.head_dim * w.num_heads * vis
         self.family = "pa_tc" if w.q_len * w.group_size >= TC_MIN_ROWS else "pa_attn"
 
+    def free(self):
+        """Drop the device buffers (the caller then empties torch's cache)."""
+        for name in ("caches", "inp", "out", "tmp", "es", "ml", "e2e_dev_in", "e2e_views",
+                     "e2e_out", "_call_args", "_k1_args", "_e2e_args"):
+            if hasattr(self, name):
+                delattr(self, name)
+
     def call(self, i: int):
         """One decode call on copy i % R through the public dispatch entry point of the
         C ABI (pa_decode, or pa_decode_mq for several new tokens), its arguments
@@ -268,26 +282,27 @@ class Decoder:
         if rc != 0:
             raise RuntimeError(f"decode returned {rc}")
 
-    def split_call(self, i: int, ev):
-        """The same call as its kernels, with events (start, after kernel 1, end) between them."""
-        pa, w, inp = self.pa, self.w, self.inp
-        kc, vc = self.caches[i % self.copies]
-        ev[0].record()
-        if w.q_len > 1:  # no separate phase entry points: the whole call is timed
-            self.call(i)
-            ev[1].record()
-        elif self.variant == 2:
-            pa.pa_decode_v2_phase1(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale,
-                                   w.partition_size, self.tmp, self.es, self.ml,
-                                   max_seq_len_hint=self.max_seq_len)
-            ev[1].record()
-            pa.pa_decode_v2_phase2(inp.seq_lens, self.max_seq_len, w.partition_size, self.tmp,
-                                   self.es, self.ml, self.out)
-        else:
-            pa.pa_decode_v1(inp.query, kc, vc, inp.block_tables, inp.seq_lens, w.scale, self.out,
-                            max_seq_len_hint=self.max_seq_len)
-            ev[1].record()
-        ev[2].record()
+    def kernel1_call(self, i: int):
+        """Kernel 1 of the call alone, through the C ABI with arguments marshalled once:
+        pa_decode_v2_phase1 for V2, the whole call otherwise (V1 is one kernel; the
+        multi-query V2 has no separate phase-1 entry point)."""
+        if self.w.q_len > 1 or self.variant != 2:
+            return self.call(i)
+        if not hasattr(self, "_k1_args"):
+            pa, w, inp = self.pa, self.w, self.inp
+            self._k1_fn = pa.load().pa_decode_v2_phase1
+            self._k1_args = []
+            for kc, vc in self.caches:
+                args = pa._lib._shape_args(inp.query, kc, vc, inp.block_tables, inp.seq_lens,
+                                           self.max_seq_len, w.scale)
+                self._k1_args.append(tuple(args) + (
+                    int(w.partition_size), pa._lib._DTYPE[inp.query.dtype],
+                    ctypes.c_void_p(self.tmp.data_ptr()), ctypes.c_void_p(self.es.data_ptr()),
+                    ctypes.c_void_p(self.ml.data_ptr()), self.tmp.shape[-2], None))
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        rc = self._k1_fn(*self._k1_args[i % self.copies], stream)
+        if rc != 0:
+            raise RuntimeError(f"phase 1 returned {rc}")
 
     def pack_host_inputs(self):
         """One pinned host buffer holding a step's query, block tables and lengths;
@@ -438,6 +453,90 @@ def soak(dec, i0: int, seconds: float) -> int:
     return i
 
 
+def time_calls(fn, i0: int, n: int) -> float:
+    """ms per call of n back-to-back calls fn(i0 + k), between two CUDA events on the
+    current stream (the stream every launch goes to)."""
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(n):
+        fn(i0 + k)
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / n
+
+
+def roofline(dec, k1_ms: float, ms_step: float, w: wl.Workload):
+    """The dominant kernel (kernel 1) against its bound: HBM bytes or tensor FLOPs,
+    whichever takes longer at its peak."""
+    peak, peak_kind = hbm_peak()
+    tpeak, tpeak_kind = bf16_peak()
+    kernel = dec.family + ("_v2_phase1" if dec.variant == 2 else "_v1")
+    k1_gbs = dec.kv_bytes / (k1_ms * 1e-3) / 1e9
+    k1_tflops = dec.flops / (k1_ms * 1e-3) / 1e12
+    tensor_bound = dec.flops / (tpeak * 1e12) > dec.kv_bytes / (peak * 1e9)
+    if tensor_bound:
+        r = {"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2), "peak": tpeak,
+             "peak_kind": tpeak_kind + (" dense bf16 (burst)" if w.dtype == wl.BF16 else
+                                        " dense bf16 (burst) x 1, fp16's nominal ratio"),
+             "unit": "TFLOP/s", "frac": round(k1_tflops / tpeak, 4)}
+    else:
+        r = {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2), "peak": peak,
+             "peak_kind": peak_kind + " copy bandwidth", "unit": "GB/s",
+             "frac": round(k1_gbs / peak, 4),
+             "frac_of_nominal": round(k1_gbs / NOMINAL_HBM_GBS, 4)}
+    split = w.q_len == 1 and dec.variant == 2
+    r |= {"traffic": recorded_traffic(w.name, kernel),
+          "algorithmic_bytes_per_launch": dec.kv_bytes,
+          "algorithmic_flops_per_launch": dec.flops,
+          "kernel_us": round(k1_ms * 1e3, 3),
+          "timing": ("kernel 1 alone: pa_decode_v2_phase1 called back to back between two CUDA "
+                     "events on its stream, so consecutive launches keep the programmatic "
+                     "dependent launch overlap they have inside the timed call")
+                    if split else
+                    "the whole call (its one kernel for V1; both kernels for the multi-query V2), "
+                    "the timed region's own events",
+          "merge_us": round(max(0.0, ms_step - k1_ms) * 1e3, 3) if split else None}
+    return r
+
+
+def measure(dec, w: wl.Workload, i0: int, K: int, W: int, world: int, local: int):
+    """W warm-up calls, then the timed region (K calls, barrier and synchronize on both
+    sides, clocks sampled under load) and kernel 1 alone over K calls after it.
+    Returns (ms per call over the slowest rank, kernel-1 ms per launch, clocks, next i)."""
+    for k in range(W):
+        dec.call(i0 + k)
+    torch.cuda.synchronize()
+    i = i0 + W
+    with ClockSampler(local) as clk:
+        # keep the GPU loaded around the timed region so the clock samples describe it
+        i = soak(dec, i, 1.0)
+        barrier(world)
+        torch.cuda.synchronize()
+        ms_step = time_calls(dec.call, i, K)
+        barrier(world)
+        i += K
+        for k in range(W):
+            dec.kernel1_call(i + k)
+        i += W
+        k1_ms = time_calls(dec.kernel1_call, i, K)
+        i += K
+        i = soak(dec, i, 0.5)
+    clocks = clk.summary()
+    return max_over_ranks(ms_step, world, dec.device), k1_ms, clocks, i
+
+
+def config_line(dec, w: wl.Workload, ms_step: float, k1_ms: float, clocks, world: int):
+    """The per-workload fields shared by the headline and the per_config entries."""
+    peak, _ = hbm_peak()
+    gbs = world * dec.kv_bytes / (ms_step * 1e-3) / 1e9
+    return {"us_per_call": round(ms_step * 1e3, 3), "value": round(gbs, 2), "unit": "GB/s",
+            "pct_of_hbm_peak": round(100.0 * gbs / world / peak, 2),
+            "pct_of_nominal_hbm": round(100.0 * gbs / world / NOMINAL_HBM_GBS, 2),
+            "variant": f"v{dec.variant}", "kv_bytes_per_step": dec.kv_bytes,
+            "roofline": roofline(dec, k1_ms, ms_step, w), "clocks": clocks}
+
+
 def time_gpu(args, w: wl.Workload):
     world, rank, local = dist_env()
     init_dist(world, "nccl")
@@ -446,37 +545,8 @@ def time_gpu(args, w: wl.Workload):
     dec = Decoder(w, device)
     K, W = args.steps, args.warmup
 
-    for i in range(W):
-        dec.call(i)
-    torch.cuda.synchronize()
-
-    with ClockSampler(local) as clk:
-        # keep the GPU loaded around the timed region so the clock samples describe it
-        i = soak(dec, W, 1.0)
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record()
-        for k in range(K):
-            dec.call(i + k)
-        t1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        # kernel breakdown: the same calls split into their kernels, events between them
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-        i += K
-        for k in range(K):
-            dec.split_call(i + k, evs[k])
-        torch.cuda.synchronize()
-        soak(dec, i + K, 0.5)
-    clocks = clk.summary()
-
-    total_ms = t0.elapsed_time(t1)
-    k1_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    k2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    total_ms = max_over_ranks(total_ms, world, device)
-    ms_step = total_ms / K
+    ms_step, k1_ms, clocks, _ = measure(dec, w, 0, K, W, world, local)
+    head = config_line(dec, w, ms_step, k1_ms, clocks, world)
 
     # End to end through the public API with host buffers: each step copies its
     # inputs (query, block tables, sequence lengths, packed in one pinned
@@ -492,67 +562,69 @@ def time_gpu(args, w: wl.Workload):
     h2d = host_in.numel()
     d2h = dec.e2e_host_out[0].numel() * dec.e2e_host_out[0].element_size()
 
-    gbs = world * dec.kv_bytes / (ms_step * 1e-3) / 1e9
-    peak, peak_kind = hbm_peak()
-    tpeak, tpeak_kind = bf16_peak()
-    kernel = dec.family + ("_v2_phase1" if dec.variant == 2 else "_v1")
-    k1_gbs = dec.kv_bytes / (k1_ms * 1e-3) / 1e9
-    k1_tflops = dec.flops / (k1_ms * 1e-3) / 1e12
-    traffic = recorded_traffic(w.name, kernel)
-    # The bound: whichever of HBM bytes and tensor FLOPs takes longer at its peak.
-    tensor_bound = dec.flops / (tpeak * 1e12) > dec.kv_bytes / (peak * 1e9)
     result = {
         "metric": METRIC,
-        "value": round(gbs, 2),
+        "value": head["value"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": K,
         "warmup": W,
         "ms_per_step": round(ms_step, 6),
-        "us_per_call": round(ms_step * 1e3, 3),
-        "pct_of_hbm_peak": round(100.0 * gbs / world / peak, 2),
+        "us_per_call": head["us_per_call"],
+        "pct_of_hbm_peak": head["pct_of_hbm_peak"],
+        "pct_of_nominal_hbm": head["pct_of_nominal_hbm"],
+        "peaks": {"hbm_gbs": hbm_peak()[0], "hbm_kind": hbm_peak()[1] + " copy bandwidth "
+                  "(read + write)", "nominal_hbm_gbs": NOMINAL_HBM_GBS},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": wl.DTYPE_NAME[w.dtype],
         "data": "synthetic (seeded N(0,1) queries and paged K/V caches, random block placement)",
-        "config": {
-            "workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
-            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-            "partition_size": w.partition_size, "max_seq_len": dec.max_seq_len,
-            "sum_seq_len": int(dec.inp.seq_lens.sum().item()), "kv_bytes_per_step": dec.kv_bytes,
-            "variant": f"v{dec.variant}", "accumulate": "f32",
-            "l2": (f"inputs larger than L2: {dec.copies} rotating K/V cache copies, "
-                   f"{dec.copies * dec.kv_bytes / 1e6:.0f} MB read between reuses vs 129 MB L2"),
-            "parallelism": "replicas" if world > 1 else "single GPU",
-        },
+        "config": workload_config(dec, w, world),
         "e2e": {"value": round(world * dec.kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d,
                 "pipelined": "two buffer sets; step k + 1's input copy and step k - 1's output copy overlap step k's decode",
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": K * dec.launches_per_step,
-        "roofline": ({"bound": "tensor", "kernel": kernel, "achieved": round(k1_tflops, 2),
-                      "peak": tpeak,
-                      "peak_kind": tpeak_kind + (" dense bf16 (burst)" if w.dtype == wl.BF16 else
-                                                 " dense bf16 (burst) x 1, fp16's nominal ratio"),
-                      "unit": "TFLOP/s", "frac": round(k1_tflops / tpeak, 4)}
-                     if tensor_bound else
-                     {"bound": "hbm", "kernel": kernel, "achieved": round(k1_gbs, 2),
-                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                      "frac": round(k1_gbs / peak, 4)}) | {
-                     "traffic": traffic,
-                     "algorithmic_bytes_per_launch": dec.kv_bytes,
-                     "algorithmic_flops_per_launch": dec.flops,
-                     "kernel_us": round(k1_ms * 1e3, 3),
-                     "timing": ("kernel 1 alone, CUDA events around it on its stream, "
-                                "averaged over K split calls right after the timed region")
-                               if w.q_len == 1 else
-                               "whole call (its one or two kernels), CUDA events, K calls after "
-                               "the timed region",
-                     "merge_us": round(k2_ms * 1e3, 3) if dec.variant == 2 else None},
+        "roofline": head["roofline"],
         "clocks": clocks,
     }
-    return result, dec, rank, world
+    del host_in
+    dec.free()
+    del dec
+    torch.cuda.empty_cache()
+
+    # The other decode workloads the >= 70% target names (the 100K-token sequence
+    # at both partition sizes) and the largest one, each timed the same way after
+    # the headline's timed region, within the same process.
+    if not args.no_per_config and world == 1:
+        per = {}
+        for name in PER_CONFIG:
+            if name == w.name:
+                continue
+            wc = wl.ALL[name]
+            d = Decoder(wc, device)
+            ms_c, k1_c, clk_c, _ = measure(d, wc, 0, K, W, world, local)
+            per[name] = config_line(d, wc, ms_c, k1_c, clk_c, world) | {
+                "config": workload_config(d, wc, world)}
+            d.free()
+            del d
+            torch.cuda.empty_cache()
+        result["per_config"] = per
+    return result, rank, world
+
+
+def workload_config(dec, w: wl.Workload, world: int):
+    return {
+        "workload": w.name, "num_seqs": w.num_seqs, "num_heads": w.num_heads,
+        "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+        "partition_size": w.partition_size, "q_len": w.q_len, "max_seq_len": dec.max_seq_len,
+        "sum_seq_len": dec.sum_seq_len, "kv_bytes_per_step": dec.kv_bytes,
+        "variant": f"v{dec.variant}", "accumulate": "f32",
+        "l2": (f"inputs larger than L2: {dec.copies} rotating K/V cache copies, "
+               f"{dec.copies * dec.kv_bytes / 1e6:.0f} MB read between reuses vs 129 MB L2"),
+        "parallelism": "replicas" if world > 1 else "single GPU",
+    }
 
 
 # ---------------------------------------------------------------- the oracle on the host
@@ -605,6 +677,8 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.ALL))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (no per_config entries)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -628,7 +702,7 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
-    result, dec, rank, world = time_gpu(args, w)
+    result, rank, world = time_gpu(args, w)
     if rank == 0:
         if not args.no_cpu_baseline:
             gbs, cores, desc, _ = time_oracle(w)

@@ -13,7 +13,10 @@
 // every GPU that loads the library holds it until the process exits.  In
 // host code its name is only a stand-in, so its device address is looked
 // up with cudaGetSymbolAddress once per device, with that device current,
-// on the first call made on that device.
+// on the first call made on that device, and kept for the life of the
+// process.  A cudaDeviceReset unloads the library's device code, so the
+// kept address would then be stale: this entry point must not be called on
+// a device after that device has been reset.
 #include <atomic>
 #include <cstdint>
 
@@ -60,10 +63,15 @@ extern "C" PA_API int pa_decode_v2_static(const void *query, const void *key_cac
     const long long full = (long long)max_blocks_per_seq * block_size;
     const long long cap = (max_seq_len_hint > 0 && max_seq_len_hint < full) ? max_seq_len_hint : full;
     const long long np = (cap + partition_size - 1) / partition_size;
-    const long long rows = (long long)num_seqs * num_heads * np;
-    if (np < 1 || np > INT32_MAX ||
-        rows * (head_dim + 2) * (long long)sizeof(float) > (long long)PA_STATIC_SCRATCH_BYTES)
+    // rows * (head_dim + 2) * 4 bytes must fit the array, rows = num_seqs *
+    // num_heads * np.  Compared by successive division, which cannot overflow:
+    // for positive integers, np <= floor(floor(R / H) / S) exactly when
+    // np * H * S <= R.
+    const long long max_rows = (long long)PA_STATIC_SCRATCH_BYTES /
+                               (((long long)head_dim + 2) * (long long)sizeof(float));
+    if (np < 1 || np > INT32_MAX || np > max_rows / num_heads / num_seqs)
         return PA_ERR_WORKSPACE;
+    const long long rows = (long long)num_seqs * num_heads * np;
 
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)

@@ -133,7 +133,8 @@ def test_multi_query_dispatch_validation(cuda_lib):
 def test_rows_kernel_override_validation(cuda_lib):
     lib = cuda_lib.load()
     assert lib.pa_set_rows_kernel(-1) == 1
-    assert lib.pa_set_rows_kernel(5) == 1
+    assert lib.pa_set_rows_kernel(6) == 1
+    assert lib.pa_set_rows_kernel(5) == 0
     assert lib.pa_set_rows_kernel(4) == 0
     assert lib.pa_set_rows_kernel(2) == 0
     assert lib.pa_set_rows_kernel(0) == 0
@@ -155,3 +156,32 @@ def test_binding_refuses_cpu_tensors(cuda_lib):
     with pytest.raises(ValueError):
         cuda_lib.pa_decode_v1(inp.query, inp.key_cache, inp.value_cache, inp.block_tables,
                               inp.seq_lens, 0.088, out)
+
+
+def _static(lib, **kw):
+    a = dict(num_seqs=1, num_heads=8, num_kv_heads=2, head_dim=128, num_blocks=128, block_size=16,
+             max_blocks=63, hint=0, partition_size=512)
+    a.update(kw)
+    fn = lib.pa_decode_v2_static
+    P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P, P]
+    fn.restype = I
+    return fn(FAKE, FAKE, FAKE, FAKE, FAKE, a["num_seqs"], a["num_heads"], a["num_kv_heads"],
+              a["head_dim"], a["num_blocks"], a["block_size"], a["max_blocks"], a["hint"], 0.088,
+              a["partition_size"], 0, FAKE, None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    # products far past 2^63 if multiplied out: must be rejected, not wrapped
+    dict(num_seqs=2**31 - 1, num_heads=2**31 - 1, max_blocks=2**31 - 1, block_size=1,
+         partition_size=1),
+    dict(num_seqs=65535, num_heads=65535 * 64, num_kv_heads=65535, max_blocks=2**30, block_size=2),
+    dict(head_dim=2**31 - 3),
+    # just past the 16 MiB array: 32 x 32 x 32 partitions x 130 x 4 B = 17.0 MB
+    dict(num_seqs=32, num_heads=32, num_kv_heads=8, max_blocks=1024, partition_size=512),
+])
+def test_static_entry_rejects_sizes_beyond_its_array_on_the_host(cuda_lib, kw):
+    """The no-allocation entry point refuses, before any CUDA call, every size whose
+    intermediates would not fit its array -- including sizes whose byte count would
+    overflow a 64-bit product."""
+    assert _static(cuda_lib.load(), **kw) == cuda_lib.PA_ERR_WORKSPACE
