@@ -51,6 +51,8 @@ NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = {
     "pa_attn": ["paged_kv_decode_v2_gb300/csrc/pa_attn.cuh",
                 "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
+    "pa_simt": ["paged_kv_decode_v2_gb300/csrc/pa_simt.cuh",
+                "paged_kv_decode_v2_gb300/csrc/pa_device.cuh"],
     "pa_tc": ["paged_kv_decode_v2_gb300/csrc/pa_tc.cuh",
               "paged_kv_decode_v2_gb300/csrc/pa_tc2.cuh",
               "paged_kv_decode_v2_gb300/csrc/pa_tcgen05.cuh",
@@ -58,6 +60,8 @@ KERNEL_SOURCES = {
 }
 # From this many query rows per KV head the library runs the tcgen05 kernel.
 TC_MIN_ROWS = 32
+# pa_set_rows_kernel mode of this run (--rows-kernel).
+ROWS_KERNEL = 0
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -250,7 +254,9 @@ class Decoder:
             for i in range(w.q_len):
                 vis += max(0, min(L - w.q_len + i + 1, L))
         self.flops = 4 * w.head_dim * w.num_heads * vis
-        self.family = "pa_tc" if w.q_len * w.group_size >= TC_MIN_ROWS else "pa_attn"
+        rows = w.q_len * w.group_size
+        self.family = ("pa_tc" if rows >= TC_MIN_ROWS else
+                       "pa_simt" if rows <= 8 and ROWS_KERNEL == 5 else "pa_attn")
 
     def free(self):
         """Drop the device buffers (the caller then empties torch's cache)."""
@@ -677,6 +683,9 @@ def main():
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(wl.ALL))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows-kernel", type=int, default=0, choices=range(6),
+                    help="pa_set_rows_kernel mode (0 = the library's choice; 5 = the CUDA-core "
+                         "kernel up to 8 query rows per KV head)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the chosen workload (no per_config entries)")
     args = ap.parse_args()
@@ -702,7 +711,14 @@ def main():
         print(json.dumps(line), flush=True)
         return
 
+    global ROWS_KERNEL
+    ROWS_KERNEL = args.rows_kernel
+    if ROWS_KERNEL:
+        import paged_kv_decode_v2_gb300 as pa
+        pa.pa_set_rows_kernel(ROWS_KERNEL)
     result, rank, world = time_gpu(args, w)
+    if ROWS_KERNEL:
+        result["rows_kernel"] = ROWS_KERNEL
     if rank == 0:
         if not args.no_cpu_baseline:
             gbs, cores, desc, _ = time_oracle(w)

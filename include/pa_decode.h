@@ -150,6 +150,38 @@ PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *va
                         int32_t *status, pa_stream_t stream);
 
 /*
+ * Single-kernel V2: the same result as pa_decode_v2 (within the stated
+ * tolerances; the merge sums in another order), with phase 2 done inside
+ * the phase-1 grid.  Each CTA writes its partition's partials, then takes a
+ * ticket from counters[b * num_kv_heads + k]; the CTA that takes the last
+ * ticket of its (sequence b, KV head k) merges that group's partitions into
+ * out -- the single-kernel alternative to the separate reduction pass that
+ * "paged_attn.py" commit 490ff98 sets against CCCL's two-pass dispatch
+ * ("Architecture follows CCCL's two-pass dispatch", "vllm/_custom_ops.py"
+ * commit 900ae0b).  The merging CTA reads partitions in index order, so the
+ * output does not depend on which CTA finishes last.
+ *   counters  [num_seqs, num_kv_heads] int32, device memory owned by the
+ *             caller, all zero before the first call; every call that
+ *             completes leaves them zero again (each counter wraps to 0 on
+ *             its last ticket), so one zeroing at allocation suffices.  Calls
+ *             that overlap on the GPU must not share a counters array.
+ * The other arguments are pa_decode_v2's; tmp_output, exp_sums and
+ * max_logits hold the partials afterwards exactly as after pa_decode_v2.
+ * Runs on the mma.sync kernel whatever the group size (no tcgen05 or SIMT
+ * variant).  Measured against pa_decode_v2 on this GPU it is slower on the
+ * decode workloads (see the project's design notes), so pa_decode never
+ * picks it; it is a separate entry point.
+ */
+PA_API int pa_decode_v2_fused(const void *query, const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, int max_blocks_per_seq, int max_seq_len_hint,
+                              float scale, int partition_size, int dtype, void *out,
+                              float *tmp_output, float *exp_sums, float *max_logits,
+                              int max_num_partitions, int32_t *counters, int32_t *status,
+                              pa_stream_t stream);
+
+/*
  * Phase 1 alone: writes tmp_output, exp_sums and max_logits for every
  * partition (same arguments as pa_decode_v2 without `out`).
  */
@@ -248,6 +280,13 @@ PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *va
 /*
  * Which variant pa_decode runs for these sizes on the current device:
  * returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.  Host only.
+ * The rule: V1 when ceil(max_seq_len / partition_size) <= 1 (a merge of one
+ * partition would only copy), else V2.  num_seqs and num_kv_heads are
+ * validated (> 0) but are reserved: they do not change the answer.  A
+ * grid-fill rule (V1 once num_seqs * num_kv_heads CTAs fill the device) was
+ * measured on this GPU and lost to V2 in every regime with more than one
+ * partition (512 sequences of <= 1024 tokens: V2 177 us, V1 196 us), so the
+ * two counts are kept in the signature for a future rule and ignored now.
  */
 PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size);
 
@@ -282,7 +321,9 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
  * <= 128 and sequences reach 1024 tokens, else one tile and two CTAs per
  * SM); 1 always the mma.sync kernel; 2 always a tcgen05 kernel; 3 always
  * the one-tile tcgen05 kernel; 4 always the two-tile one (one tile for
- * head_dim 256).  Either kernel computes the same
+ * head_dim 256); 5 the CUDA-core kernel (Q.K and the softmax reduced with
+ * warp shuffles, P.V as scalar FMAs, no tensor-core instruction) up to 8
+ * rows, else as 0.  Either kernel computes the same
  * result within the stated tolerances; the choice changes only speed.  The
  * tcgen05 kernel takes its K ring stages from pa_set_launch_config's
  * stages_per_warp and its V ring stages from warps_per_cta when those are
@@ -315,7 +356,10 @@ PA_API int pa_set_rows_kernel(int mode);
  *     Larger calls return PA_ERR_WORKSPACE and launch nothing.
  *   - Set-up: the first call on a device looks up the array's device
  *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture.
+ *     first call before any stream capture.  The address is kept for the
+ *     life of the process, so do not call this entry point on a device
+ *     after cudaDeviceReset on it (the reset unloads the array and the kept
+ *     address goes stale).
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's contents.  No slot needs clearing (each slot the merge
  *     reads is written earlier in the same call), but two calls that

@@ -55,6 +55,8 @@ def load() -> ctypes.CDLL:
     lib.pa_v2_workspace_bytes.restype = S
     lib.pa_decode_v2.argtypes = attn + [I, I, P, P, P, P, I, P, P]
     lib.pa_decode_v2.restype = I
+    lib.pa_decode_v2_fused.argtypes = attn + [I, I, P, P, P, P, I, P, P, P]
+    lib.pa_decode_v2_fused.restype = I
     lib.pa_decode_v2_phase1.argtypes = attn + [I, I, P, P, P, I, P, P]
     lib.pa_decode_v2_phase1.restype = I
     lib.pa_decode_v2_phase2.argtypes = [P, I, I, I, I, I, I, P, P, P, I, P, P, P]
@@ -166,6 +168,27 @@ def pa_decode_v2(query, key_cache, value_cache, block_tables, seq_lens, scale, p
     return out
 
 
+def alloc_counters(num_seqs: int, num_kv_heads: int, device="cuda"):
+    """The zeroed ticket counters pa_decode_v2_fused needs: [num_seqs, num_kv_heads] int32.
+    Every completed call leaves them zero again, so they are allocated once."""
+    return torch.zeros((num_seqs, num_kv_heads), dtype=torch.int32, device=device)
+
+
+def pa_decode_v2_fused(query, key_cache, value_cache, block_tables, seq_lens, scale,
+                       partition_size, out, tmp_output, exp_sums, max_logits, counters,
+                       max_seq_len_hint=0, status=None, stream=None):
+    """pa_decode_v2 in one kernel: the last CTA of each (sequence, KV head) merges."""
+    lib = load()
+    args = _shape_args(query, key_cache, value_cache, block_tables, seq_lens, max_seq_len_hint, scale)
+    if counters.dtype != torch.int32 or not counters.is_cuda or counters.numel() < args[5] * args[7]:
+        raise ValueError("counters must be a CUDA int32 tensor of num_seqs * num_kv_heads zeros")
+    rc = lib.pa_decode_v2_fused(*args, int(partition_size), _DTYPE[query.dtype], _ptr(out),
+                                _ptr(tmp_output), _ptr(exp_sums), _ptr(max_logits),
+                                tmp_output.shape[2], _ptr(counters), _ptr(status), _stream(stream))
+    _check("pa_decode_v2_fused", rc)
+    return out
+
+
 def pa_decode_v2_phase1(query, key_cache, value_cache, block_tables, seq_lens, scale,
                         partition_size, tmp_output, exp_sums, max_logits, max_seq_len_hint=0,
                         status=None, stream=None):
@@ -268,7 +291,8 @@ def pa_set_launch_config(warps_per_cta: int = 0, stages_per_warp: int = 0) -> No
 
 def pa_set_rows_kernel(mode: int = 0) -> None:
     """0: by query rows per KV head; 1: always mma.sync; 2: always tcgen05; 3: tcgen05, one
-    query tile per CTA; 4: tcgen05, two query tiles per CTA."""
+    query tile per CTA; 4: tcgen05, two query tiles per CTA; 5: the CUDA-core (SIMT) kernel
+    up to 8 rows per KV head, else as 0."""
     _check("pa_set_rows_kernel", load().pa_set_rows_kernel(mode))
 
 

@@ -20,7 +20,8 @@ std::atomic<int> g_tune_warps{0};
 std::atomic<int> g_tune_stages{0};
 // Kernel for the query rows of a KV head: 0 = by row count, 1 = always the
 // mma.sync kernel, 2 = always a tcgen05 kernel (query tiles by row count),
-// 3 = the one-tile tcgen05 kernel, 4 = the two-tile one (head_dim <= 128).
+// 3 = the one-tile tcgen05 kernel, 4 = the two-tile one (head_dim <= 128),
+// 5 = the CUDA-core (SIMT) kernel up to 8 rows, else as 0.
 std::atomic<int> g_rows_kernel{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
@@ -171,15 +172,24 @@ int encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_bloc
     return PA_OK;
 }
 
-// Index of a kernel instantiation: storage type x head_dim x block size x n-tiles x V1/V2.
-constexpr int kKernelSlots = 2 * 3 * 4 * 2 * 2;
+// Index of a kernel instantiation: storage type x head_dim x block size x
+// row variant (mma.sync with one or two n-tiles, or the SIMT kernel padded
+// to 1, 2, 4 or 8 rows) x V2 / V1 / fused V2.
+constexpr int kKernelSlots = 2 * 3 * 4 * 6 * 3;
 
-int kernel_slot(int dtype, int head_dim, int block_size, int group, bool v1)
+int kernel_slot(const AttnLaunch &L)
 {
-    const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
-    const int bi = block_size == 8 ? 3 : block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
-    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 2 + (group > 8 ? 1 : 0)) * 2 +
-           (v1 ? 1 : 0);
+    const int di = L.head_dim == 64 ? 0 : L.head_dim == 128 ? 1 : 2;
+    const int bi = L.block_size == 8 ? 3 : L.block_size == 16 ? 0 : L.block_size == 32 ? 1 : 2;
+    const int c = L.cta_cols;
+    const int vi = L.simt ? (c <= 1 ? 2 : c <= 2 ? 3 : c <= 4 ? 4 : 5) : (c > 8 ? 1 : 0);
+    return ((((L.dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 6 + vi) * 3 + attn_variant(L);
+}
+
+// The kernel table of a launch: the SIMT or the mma.sync kernels.
+const AttnOps *ops_of(const AttnLaunch &L)
+{
+    return L.simt ? simt_ops(L.dtype, L.head_dim) : attn_ops(L.dtype, L.head_dim);
 }
 
 // Per-device, per-kernel dynamic shared memory limit after the opt-in (0 = not yet).
@@ -191,7 +201,7 @@ std::atomic<int> g_occ[kMaxDevices][kKernelSlots][kMaxWarps + 1][kMaxStages + 1]
 // device) and returns that limit, or 0 on error.
 size_t smem_limit(int dev, const AttnLaunch &L)
 {
-    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.cta_cols, L.v1);
+    const int slot = kernel_slot(L);
     const int have = g_smem_limit[dev][slot].load(std::memory_order_acquire);
     if (have > 0)
         return (size_t)have;
@@ -199,8 +209,7 @@ size_t smem_limit(int dev, const AttnLaunch &L)
     if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 0;
     size_t limit = 0;
-    cudaError_t e = attn_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.cta_cols, L.v1, optin,
-                                                           &limit);
+    cudaError_t e = ops_of(L)->prepare(L.block_size, L.cta_cols, attn_variant(L), optin, &limit);
     if (e != cudaSuccess)
         return 0;
     g_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
@@ -217,11 +226,11 @@ int occupancy(int dev, const AttnLaunch &L, int warps, int stages, size_t limit)
     const size_t smem = attn_smem(L, warps, stages);
     if (smem > limit || warps < 1 || warps > kMaxWarps || stages < 1 || stages > kMaxStages)
         return 0;
-    const int slot = kernel_slot(L.dtype, L.head_dim, L.block_size, L.cta_cols, L.v1);
+    const int slot = kernel_slot(L);
     const int c = g_occ[dev][slot][warps][stages].load(std::memory_order_relaxed);
     if (c)
         return c - 1;
-    const int n = attn_ops(L.dtype, L.head_dim)->occupancy(L.block_size, L.cta_cols, L.v1, warps, smem);
+    const int n = ops_of(L)->occupancy(L.block_size, L.cta_cols, attn_variant(L), warps, smem);
     g_occ[dev][slot][warps][stages].store(n + 1, std::memory_order_relaxed);
     return n;
 }
@@ -350,7 +359,7 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
     size_attn(L, dev, sms, limit);
     if (L.smem_bytes > limit)
         return PA_ERR_UNSUPPORTED;
-    cudaError_t e = attn_ops(L.dtype, L.head_dim)->launch(L, stream);
+    cudaError_t e = ops_of(L)->launch(L, stream);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -358,7 +367,9 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
 bool use_tc(int cols)
 {
     const int mode = g_rows_kernel.load(std::memory_order_relaxed);
-    return mode >= 2 || (mode == 0 && cols >= kTcMinRows);
+    if (mode >= 2 && mode <= 4)
+        return true;
+    return (mode == 0 || mode == 5) && cols >= kTcMinRows;
 }
 
 // 128-row query tiles per CTA of the tcgen05 kernel.  Two tiles (one CTA per
@@ -398,9 +409,11 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
                int max_blocks_per_seq, int cap, float scale, int dtype, bool v1,
                int num_partitions, int partition_size,
                float *tmp_output, float *exp_sums, float *max_logits, int max_num_partitions,
-               void *out, int32_t *status)
+               void *out, int32_t *status, int32_t *counters = nullptr)
 {
     L = AttnLaunch{};
+    // The fused V2 (counters given) runs on the mma.sync kernel at any row count.
+    const bool fused = counters != nullptr;
     int rc = encode_cache_map(&L.tmap_k, key_cache, dtype, num_blocks, num_kv_heads, block_size,
                               head_dim);
     if (rc)
@@ -418,16 +431,18 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.group = num_heads / num_kv_heads;
     p.q_len = q_len;
     p.cols = p.group * q_len;
-    L.tc = use_tc(p.cols);
+    L.tc = !fused && use_tc(p.cols);
     if (L.tc) {
         // 128 rows per query tile; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
         L.tc_tiles = tc_tiles(p.cols, head_dim, dtype, cap);
         p.col_groups = row_ctas(p.cols, head_dim, dtype, cap);
     } else {
-        // Up to 8 query rows: one n-tile; more: 16 per CTA, split over CTAs.
+        // Up to 8 query rows: one n-tile (or the SIMT kernel when asked for);
+        // more: 16 per CTA, split over CTAs.
         L.cta_cols = p.cols <= 8 ? p.cols : kMaxGroup;
         p.col_groups = (p.cols + L.cta_cols - 1) / L.cta_cols;
+        L.simt = !fused && p.cols <= 8 && g_rows_kernel.load(std::memory_order_relaxed) == 5;
     }
     p.num_blocks = num_blocks;
     p.max_blocks = max_blocks_per_seq;
@@ -439,7 +454,9 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.exp_sums = exp_sums;
     p.max_logits = max_logits;
     p.out = out;
+    p.counters = counters;
     p.status = status;
+    L.fused = fused;
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.dtype = dtype;
@@ -464,7 +481,8 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
                    int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
                    int max_blocks_per_seq, int max_seq_len_hint, float scale, int partition_size,
                    int dtype, float *tmp_output, float *exp_sums, float *max_logits,
-                   int max_num_partitions, int32_t *status, cudaStream_t stream, int *cap_out)
+                   int max_num_partitions, int32_t *status, cudaStream_t stream, int *cap_out,
+                   void *fused_out = nullptr, int32_t *counters = nullptr)
 {
     int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                          num_heads, num_kv_heads, head_dim, num_blocks, block_size,
@@ -493,7 +511,7 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
     rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
                     num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
                     cap, scale, dtype, false, np, partition_size, tmp_output, exp_sums, max_logits,
-                    max_num_partitions, nullptr, status);
+                    max_num_partitions, fused_out, status, counters);
     if (rc)
         return rc;
     return prepare_and_launch_attn(L, stream);
@@ -547,6 +565,8 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
 
 int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size, int sms)
 {
+    // num_seqs, num_kv_heads and the SM count are reserved (the header says
+    // so): a grid-fill rule built on them lost to the rule below.
     (void)num_seqs;
     (void)num_kv_heads;
     (void)sms;
@@ -660,6 +680,26 @@ PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *va
                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype, out,
                            tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
+}
+
+PA_API int pa_decode_v2_fused(const void *query, const void *key_cache, const void *value_cache,
+                              const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
+                              int num_heads, int num_kv_heads, int head_dim, int num_blocks,
+                              int block_size, int max_blocks_per_seq, int max_seq_len_hint,
+                              float scale, int partition_size, int dtype, void *out,
+                              float *tmp_output, float *exp_sums, float *max_logits,
+                              int max_num_partitions, int32_t *counters, int32_t *status,
+                              pa_stream_t stream)
+{
+    if (!out || !aligned(out, 4) || !counters || !aligned(counters, 4))
+        return PA_ERR_INVALID_ARG;
+    int cap = 0;
+    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, 1,
+                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
+                            tmp_output, exp_sums, max_logits, max_num_partitions, status,
+                            (cudaStream_t)stream, &cap, out, counters);
+    return rc;
 }
 
 PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void *value_cache,
@@ -817,7 +857,7 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp)
 
 PA_API int pa_set_rows_kernel(int mode)
 {
-    if (mode < 0 || mode > 4)
+    if (mode < 0 || mode > 5)
         return PA_ERR_INVALID_ARG;
     g_rows_kernel.store(mode, std::memory_order_relaxed);
     return PA_OK;

@@ -34,6 +34,14 @@
 //     tmp_output = sum exp(s - m_p) V / l_p
 // ("paged_attention_v2_pytorch.py" commit 9cb7f9d, "Implementation",
 // Phase 1).  V1 writes out = o / l rounded to the storage type.
+//
+// FUSED (V2 only) adds phase 2 to the same grid: after writing its
+// partials, each CTA takes a ticket from a per-(sequence, KV head) counter,
+// and the CTA that takes the last one merges that group's partitions into
+// out -- the single-kernel alternative to the separate reduction pass that
+// "paged_attn.py" commit 490ff98 sets against CCCL's two-pass dispatch.
+// The merging CTA reads the partitions in index order, so the result does
+// not depend on which CTA finishes last.
 #pragma once
 
 #include "pa_device.cuh"
@@ -51,7 +59,7 @@ struct AttnBounds {
     static constexpr int kMinBlocks = kNarrow ? 3 : 1;
 };
 
-template <typename T, int D, int BS, int NT, bool V1>
+template <typename T, int D, int BS, int NT, bool V1, bool FUSED = false>
 __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
                                   AttnBounds<D, NT, V1>::kMinBlocks)
     attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
@@ -156,8 +164,17 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             set_status(p.status, PA_STATUS_BAD_SEQ_LEN);
         L = L < 0 ? 0 : p.seq_len_cap;
     }
-    if (!V1 && tokA >= L)
-        return; // partition past the end of this sequence: nothing to write
+    if (!V1 && tokA >= L) {
+        // Partition past the end of this sequence: nothing to write -- except
+        // in the fused form for an empty sequence, whose zero output row no
+        // merge would write: partition 0's CTAs write it.
+        if (FUSED && part == 0 && L == 0) {
+            T *out = static_cast<T *>(p.out);
+            for (int idx = threadIdx.x; idx < ncols * D; idx += blockDim.x)
+                out[col_row(idx / D) * D + idx % D] = E::from_float(0.f);
+        }
+        return;
+    }
     // Token positions below are counted from tok0, the first token of block blk0;
     // the range is [lo, ntok) of them.
     const int tok0 = blk0 * BS;
@@ -517,33 +534,99 @@ __global__ void __launch_bounds__(AttnBounds<D, NT, V1>::kThreads,
             }
         }
     }
+
+    if constexpr (!V1 && FUSED) {
+        // ---- phase 2 in the last CTA of this (sequence, KV head).  Each
+        // thread's partial writes are made visible device-wide before the
+        // ticket is taken; the ticket counter wraps to 0 on the last ticket,
+        // which leaves it ready for the next call.
+        __shared__ int s_last;
+        __threadfence();
+        __syncthreads();
+        const int np_b = (L + p.partition_size - 1) / p.partition_size;
+        if (threadIdx.x == 0) {
+            const unsigned total = (unsigned)np_b * (unsigned)p.col_groups;
+            unsigned *ctr = reinterpret_cast<unsigned *>(p.counters) +
+                            (size_t)b * p.num_kv_heads + kv;
+            s_last = atomicInc(ctr, total - 1u) == total - 1u;
+        }
+        __syncthreads();
+        if (!s_last)
+            return;
+        __threadfence();
+        // One (query row, 4 dims) per thread and pass, over every row of the
+        // KV head (all column groups): M = max m_p, w_p = exp(m_p - M) l_p,
+        // out = sum w_p o_p / sum w_p, with M raised as larger maxima appear
+        // ("paged_attention_v2_pytorch.py" commit 9cb7f9d, "Implementation",
+        // Phase 2).  Loads bypass L1 (other CTAs wrote them in this grid).
+        for (int idx = threadIdx.x; idx < p.cols * kQuads; idx += blockDim.x) {
+            const int n = idx / kQuads;
+            const int d = (idx % kQuads) * 4;
+            const size_t bh =
+                ((size_t)b * p.q_len + n / p.group) * p.num_heads + head0 + n % p.group;
+            const float *ml = p.max_logits + bh * p.max_num_partitions;
+            const float *es = p.exp_sums + bh * p.max_num_partitions;
+            const float *tp = p.tmp_output + bh * p.max_num_partitions * D + d;
+            float m = -INFINITY, l = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int q = 0; q < np_b; ++q) {
+                const float mp = __ldcg(ml + q);
+                const float lp = __ldcg(es + q);
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(tp + (size_t)q * D));
+                if (lp == 0.f)
+                    continue;
+                const float mn = fmaxf(m, mp);
+                const float a = fast_exp2((m - mn) * kLog2e);
+                const float w = fast_exp2((mp - mn) * kLog2e) * lp;
+                acc.x = fmaf(acc.x, a, w * v.x);
+                acc.y = fmaf(acc.y, a, w * v.y);
+                acc.z = fmaf(acc.z, a, w * v.z);
+                acc.w = fmaf(acc.w, a, w * v.w);
+                l = fmaf(l, a, w);
+                m = mn;
+            }
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            T *o4 = static_cast<T *>(p.out) + bh * D + d;
+            o4[0] = E::from_float(acc.x * inv);
+            o4[1] = E::from_float(acc.y * inv);
+            o4[2] = E::from_float(acc.z * inv);
+            o4[3] = E::from_float(acc.w * inv);
+        }
+    }
 }
 
-// Kernel dispatch on block size, n-tiles (<= 8 or <= 16 columns) and V1/V2, for one head_dim.
+// Kernel dispatch on block size, n-tiles (<= 8 or <= 16 columns) and V1 /
+// V2 / fused V2, for one head_dim.  `v1` is 1 for V1, 0 for V2 and 2 for
+// the fused V2.
 template <typename T, int D>
-static const void *attn_kernel_ptr(int block_size, int cols, bool v1)
+static const void *attn_kernel_ptr(int block_size, int cols, int v1)
 {
     const bool nt2 = cols > 8;
+#define PA_PICK_NT(BS, NT)                                                                        \
+    return v1 == 1   ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, NT, true>)           \
+           : v1 == 2 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, NT, false, true>)    \
+                     : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, NT, false>);
 #define PA_PICK(BS)                                                                               \
     if (block_size == BS) {                                                                       \
-        if (nt2)                                                                                  \
-            return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 2, true>)           \
-                      : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 2, false>);         \
-        return v1 ? reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, true>)               \
-                  : reinterpret_cast<const void *>(&attn_kernel<T, D, BS, 1, false>);             \
+        if (nt2) {                                                                                \
+            PA_PICK_NT(BS, 2)                                                                     \
+        }                                                                                         \
+        PA_PICK_NT(BS, 1)                                                                         \
     }
     PA_PICK(8)
     PA_PICK(16)
     PA_PICK(32)
     PA_PICK(64)
 #undef PA_PICK
+#undef PA_PICK_NT
     return nullptr;
 }
 
 // Opts the kernel in to the largest dynamic shared memory the device allows
 // next to its static shared memory; returns that limit in *limit.
 template <typename T, int D>
-static cudaError_t attn_prepare(int block_size, int cols, bool v1, int optin_bytes, size_t *limit)
+static cudaError_t attn_prepare(int block_size, int cols, int v1, int optin_bytes, size_t *limit)
 {
     const void *fn = attn_kernel_ptr<T, D>(block_size, cols, v1);
     if (!fn)
@@ -560,7 +643,7 @@ static cudaError_t attn_prepare(int block_size, int cols, bool v1, int optin_byt
 
 // Resident CTAs per SM for a launch shape (0 on error).
 template <typename T, int D>
-static int attn_occupancy(int block_size, int cols, bool v1, int warps, size_t smem_bytes)
+static int attn_occupancy(int block_size, int cols, int v1, int warps, size_t smem_bytes)
 {
     const void *fn = attn_kernel_ptr<T, D>(block_size, cols, v1);
     int n = 0;
@@ -573,7 +656,7 @@ static int attn_occupancy(int block_size, int cols, bool v1, int warps, size_t s
 template <typename T, int D>
 static cudaError_t attn_launch(const AttnLaunch &L, cudaStream_t stream)
 {
-    const void *fn = attn_kernel_ptr<T, D>(L.block_size, L.cta_cols, L.v1);
+    const void *fn = attn_kernel_ptr<T, D>(L.block_size, L.cta_cols, attn_variant(L));
     if (!fn)
         return cudaErrorInvalidValue;
     void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),

@@ -45,7 +45,8 @@ struct AttnParams {
     float *tmp_output;           // V2: [S, q_len, H, NPcap, D]
     float *exp_sums;             // V2: [S, q_len, H, NPcap]
     float *max_logits;           // V2: [S, q_len, H, NPcap]
-    void *out;                   // V1: [S, q_len, H, D]
+    void *out;                   // V1 and fused V2: [S, q_len, H, D]
+    int32_t *counters;           // fused V2: [S, KV] tickets, zero between calls
     int32_t *status;
 };
 
@@ -57,6 +58,8 @@ struct AttnLaunch {
     int block_size;              // 8, 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
     bool v1;
+    bool fused;                  // V2 with the merge in the last CTA of each (seq, KV head)
+    bool simt;                   // the CUDA-core kernel (up to 8 rows) instead of mma.sync
     bool tc;                     // a tcgen05 kernel
     int tc_tiles;                // its 128-row query tiles per CTA (1 or 2)
     int cta_cols;                // query rows one CTA serves (<= 16): picks the n-tile count
@@ -96,9 +99,11 @@ inline size_t warp_scratch_bytes(int cta_cols, int head_dim)
 }
 
 // Entry points of the attention kernels for one (storage type, head_dim).
+// `variant`: 0 = V2 phase 1, 1 = V1, 2 = fused V2 (mma.sync kernels only).
 struct AttnOps {
-    cudaError_t (*prepare)(int block_size, int cta_cols, bool v1, int optin_bytes, size_t *limit);
-    int (*occupancy)(int block_size, int cta_cols, bool v1, int warps, size_t smem_bytes);
+    cudaError_t (*prepare)(int block_size, int cta_cols, int variant, int optin_bytes,
+                           size_t *limit);
+    int (*occupancy)(int block_size, int cta_cols, int variant, int warps, size_t smem_bytes);
     cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
 };
 const AttnOps *attn_ops_f16_d64();
@@ -108,6 +113,8 @@ const AttnOps *attn_ops_bf16_d64();
 const AttnOps *attn_ops_bf16_d128();
 const AttnOps *attn_ops_bf16_d256();
 
+inline int attn_variant(const AttnLaunch &L) { return L.v1 ? 1 : L.fused ? 2 : 0; }
+
 inline const AttnOps *attn_ops(int dtype, int head_dim)
 {
     if (dtype == PA_BF16)
@@ -115,6 +122,24 @@ inline const AttnOps *attn_ops(int dtype, int head_dim)
                                                                        : attn_ops_bf16_d256();
     return head_dim == 64 ? attn_ops_f16_d64() : head_dim == 128 ? attn_ops_f16_d128()
                                                                   : attn_ops_f16_d256();
+}
+
+// The CUDA-core (SIMT) attention kernels for up to 8 query rows per KV head:
+// same launch shape, ring and outputs as the mma.sync kernels above.
+const AttnOps *simt_ops_f16_d64();
+const AttnOps *simt_ops_f16_d128();
+const AttnOps *simt_ops_f16_d256();
+const AttnOps *simt_ops_bf16_d64();
+const AttnOps *simt_ops_bf16_d128();
+const AttnOps *simt_ops_bf16_d256();
+
+inline const AttnOps *simt_ops(int dtype, int head_dim)
+{
+    if (dtype == PA_BF16)
+        return head_dim == 64 ? simt_ops_bf16_d64() : head_dim == 128 ? simt_ops_bf16_d128()
+                                                                       : simt_ops_bf16_d256();
+    return head_dim == 64 ? simt_ops_f16_d64() : head_dim == 128 ? simt_ops_f16_d128()
+                                                                  : simt_ops_f16_d256();
 }
 
 // Dynamic shared memory of the tcgen05 kernel: the Q tile, k_stages K tiles

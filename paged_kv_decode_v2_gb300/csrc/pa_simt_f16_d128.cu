@@ -1,0 +1,7 @@
+// CUDA-core attention kernels (V2 phase 1 and V1, up to 8 query rows per
+// KV head) for f16 storage, head_dim 128.
+#include "pa_simt.cuh"
+
+namespace pa {
+PA_DEFINE_SIMT_OPS(__half, simt_ops_f16_d128, 128)
+} // namespace pa

@@ -185,3 +185,16 @@ def test_static_entry_rejects_sizes_beyond_its_array_on_the_host(cuda_lib, kw):
     intermediates would not fit its array -- including sizes whose byte count would
     overflow a 64-bit product."""
     assert _static(cuda_lib.load(), **kw) == cuda_lib.PA_ERR_WORKSPACE
+
+
+def test_fused_entry_rejects_missing_or_misaligned_counters(cuda_lib):
+    lib = cuda_lib.load()
+    args = [FAKE] * 5 + [1, 8, 2, 128, 128, 16, 63, 0, 0.088, 512, 0, FAKE, FAKE, FAKE, FAKE, 2]
+    assert lib.pa_decode_v2_fused(*args, None, None, None) == 1
+    assert lib.pa_decode_v2_fused(*args, FAKE + 2, None, None) == 1
+    bad_out = list(args)
+    bad_out[16] = None
+    assert lib.pa_decode_v2_fused(*bad_out, FAKE, None, None) == 1
+    small_ws = list(args)
+    small_ws[-1] = 1
+    assert lib.pa_decode_v2_fused(*small_ws, FAKE, None, None) == 3

@@ -91,12 +91,16 @@ CHUNKED_PREFILL = Workload("chunked_prefill", 2, 32, 8, 128, 16, 512, BF16, "fix
 # The same step with fp16 storage (run by the two-query-tile kernel).
 CHUNKED_PREFILL_F16 = CHUNKED_PREFILL.with_(name="chunked_prefill_f16", dtype=F16)
 
+# Batch decode with one query head per KV head (G = 1, 8 / 8 heads): the same
+# K/V bytes as batch_decode, one eighth of an MMA n-tile of query rows.
+BATCH_G1 = BATCH.with_(name="batch_decode_g1", num_heads=8)
+
 # The stress shape at 2 of its 8 sequences, its pool cut to match (1.07 GB of
 # K/V, still well above L2): the case ncu captures in several passes, which
 # keeps a capture's device footprint small.
 STRESS_2SEQ = STRESS.with_(name="stress_2seq", num_seqs=2, pool_blocks=17500)
 
-ALL = {w.name: w for w in (TINY, BATCH, LONG, LONG_1024, RAGGED, STRESS, STRESS_2SEQ, BATCH_SPEC4,
+ALL = {w.name: w for w in (TINY, BATCH, BATCH_G1, LONG, LONG_1024, RAGGED, STRESS, STRESS_2SEQ, BATCH_SPEC4,
                            SPEC_VERIFY16, CHUNKED_PREFILL, CHUNKED_PREFILL_F16)}
 
 
