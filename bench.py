@@ -43,6 +43,8 @@ DEFAULT_CONFIG = "batch_decode"
 # Timed after the headline in the same run: the 100K-token decode at both
 # partition sizes and the largest workload (4.3 GB of K/V).
 PER_CONFIG = ("long_100k", "long_100k_p1024", "stress")
+# Calls in each per_config timed region (the headline times --steps).
+PER_CONFIG_STEPS = 100
 # The HBM3e figure quoted for the part (about 8 TB/s); the measured copy
 # bandwidth is the roofline's denominator, this one is reported beside it.
 NOMINAL_HBM_GBS = 8000.0
@@ -459,11 +461,19 @@ def soak(dec, i0: int, seconds: float) -> int:
     return i
 
 
+# Cycles of the GPU spin that precedes a timed region (about 50 us at 2 GHz).
+SPACER_CYCLES = 100_000
+
+
 def time_calls(fn, i0: int, n: int) -> float:
     """ms per call of n back-to-back calls fn(i0 + k), between two CUDA events on the
-    current stream (the stream every launch goes to)."""
+    current stream (the stream every launch goes to).  A short GPU spin is queued
+    first, outside the timed region: the stream is then busy while the host records
+    the start event and queues the first call, so the region measures the calls
+    back to back and not the host's launch latency after an idle stream."""
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(SPACER_CYCLES)
     t0.record()
     for k in range(n):
         fn(i0 + k)
@@ -610,9 +620,9 @@ def time_gpu(args, w: wl.Workload):
                 continue
             wc = wl.ALL[name]
             d = Decoder(wc, device)
-            ms_c, k1_c, clk_c, _ = measure(d, wc, 0, K, W, world, local)
+            ms_c, k1_c, clk_c, _ = measure(d, wc, 0, PER_CONFIG_STEPS, W, world, local)
             per[name] = config_line(d, wc, ms_c, k1_c, clk_c, world) | {
-                "config": workload_config(d, wc, world)}
+                "steps": PER_CONFIG_STEPS, "config": workload_config(d, wc, world)}
             d.free()
             del d
             torch.cuda.empty_cache()

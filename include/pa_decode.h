@@ -244,20 +244,38 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
 /*
  * Which variant pa_decode_mq runs for q_len new tokens per sequence on the
  * current device: returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.
- * Host only.  V1 when one partition covers max_seq_len, or when the V1 grid
- * (num_seqs * num_kv_heads CTAs for every CTA that splits a KV head's
- * q_len * G query rows) gives every SM at least one CTA and a KV head has
- * at least 32 query rows (the tcgen05 kernel's); otherwise V2.  There is no counterpart in the
- * method's description, which dispatches single-token decode only.
+ * Host only.  With R = q_len * G query rows per KV head:
+ *   - one partition covers max_seq_len: V1;
+ *   - R < 32 (the mma.sync kernel): V2;
+ *   - 32 <= R <= 128 (the tcgen05 kernel, one query tile): V2 at the
+ *     partition size pa_decode_mq_partition returns (2048 tokens unless
+ *     partition_size is larger, or the grid would leave SMs idle), or V1
+ *     when that partition covers max_seq_len;
+ *   - R > 128 (chunked prefill): V1 when the V1 grid (num_seqs *
+ *     num_kv_heads CTAs per 128-row tile) gives every SM a CTA, else V2.
+ * There is no counterpart in the method's description, which dispatches
+ * single-token decode only; the rule is measured on GB300.
  */
 PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_kv_heads,
                                int head_dim, int max_seq_len, int partition_size);
 
 /*
+ * The partition size pa_decode_mq runs V2 with for these sizes: a multiple
+ * of partition_size by a power of two (at least partition_size; the
+ * intermediates sized for partition_size therefore always suffice), or 0
+ * when it runs V1.  Negative PA_ERR_* code for invalid arguments.  Host
+ * only.  No counterpart in the method's description.
+ */
+PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int num_kv_heads,
+                                  int head_dim, int max_seq_len, int partition_size);
+
+/*
  * pa_decode_v2_mq or pa_decode_v1_mq, as pa_decode_mq_choose picks (the
  * capacity max_seq_len_hint if > 0, else max_blocks_per_seq * block_size, is
- * its max_seq_len).  The V2 intermediates must be valid whenever V2 can be
- * chosen.
+ * its max_seq_len), V2 at the partition size pa_decode_mq_partition returns.
+ * The V2 intermediates, sized for partition_size, must be valid whenever V2
+ * can be chosen; after a V2 call they hold the partials of that (possibly
+ * coarser) partitioning.
  */
 PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
                         const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,

@@ -76,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.pa_decode_mq.restype = I
     lib.pa_decode_mq_choose.argtypes = [I, I, I, I, I, I, I]
     lib.pa_decode_mq_choose.restype = I
+    lib.pa_decode_mq_partition.argtypes = [I, I, I, I, I, I, I]
+    lib.pa_decode_mq_partition.restype = I
     lib.pa_status_string.argtypes = [I]
     lib.pa_status_string.restype = ctypes.c_char_p
     lib.pa_set_launch_config.argtypes = [I, I]
@@ -255,6 +257,16 @@ def pa_decode_mq_choose(num_seqs: int, q_len: int, num_heads: int, num_kv_heads:
                                    max_seq_len, partition_size)
     if r < 0:
         raise PagedAttentionError("pa_decode_mq_choose", -r)
+    return r
+
+
+def pa_decode_mq_partition(num_seqs: int, q_len: int, num_heads: int, num_kv_heads: int,
+                           head_dim: int, max_seq_len: int, partition_size: int) -> int:
+    """Partition size pa_decode_mq runs V2 with (0 when it runs V1)."""
+    r = load().pa_decode_mq_partition(num_seqs, q_len, num_heads, num_kv_heads, head_dim,
+                                      max_seq_len, partition_size)
+    if r < 0:
+        raise PagedAttentionError("pa_decode_mq_partition", -r)
     return r
 
 

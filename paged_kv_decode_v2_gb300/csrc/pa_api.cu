@@ -577,27 +577,58 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
     return pa_v2_num_partitions(max_seq_len, partition_size) <= 1 ? 1 : 2;
 }
 
-// Several new tokens per sequence: V1 when one partition covers the
-// sequences, or when a KV head's query rows go to the tcgen05 kernel and
-// its V1 grid (num_seqs * num_kv_heads CTAs per row split) already gives
-// every SM a CTA, so each CTA carries enough work; otherwise V2.  Measured
-// on GB300, batch decode (32 seqs up to 8192 tokens, 32 / 8 heads)
-// checking q_len tokens: q_len 2 (mma.sync): V2 92 vs V1 100 us; 4
-// (mma.sync): V2 99 vs V1 109; 8 (tcgen05): V1 151 vs V2 152; 12: V1 161
-// vs 175; 16: V1 157 vs 173; 32: V1 174 vs 235; 100K-token sequence, q_len
-// 16: V2 87 vs V1 1615 us; chunked prefill (2 x 2048 new tokens after 30K):
-// V1 2384 vs V2 4867 us.
+// Several new tokens per sequence: which variant pa_decode_mq runs, and with
+// which partition size (*part_out) if V2.
+//
+// 32 to 128 query rows per KV head (the tcgen05 kernel, one 128-row tile):
+// V2 at a coarse partition of kTcV2Partition tokens (never finer than the
+// caller's partition_size, and halved down to it while the grid would give
+// fewer CTAs than SMs), or V1 when that partition covers max_seq_len.  The
+// tcgen05 V2 pays a fixed set-up per CTA (TMEM allocation, barriers, the Q
+// tile, filling and draining its rings); 2048-token partitions amortise it
+// while still splitting the longest sequences, which bound V1.  Measured on
+// GB300 (us per call; V1 / V2 at 512 / 1024 / 2048 / 4096 tokens):
+//   32 seqs <= 8192 tokens (batch decode), 8 new tokens (32 rows):
+//     152.2 / 151.9 / 129.5 / 129.4 / 146.8
+//   the same, 16 new tokens (64 rows): 156.8 / 174.0 / 145.6 / 141.6 / 159.0
+//   the same, 32 new tokens (128 rows): 175.7 / 235.6 / 187.0 / 177.1 / 193.6
+//   one 100K-token sequence, 4 new tokens (32 rows): V2 55.2 / 54.3 / 49.5 / 69.9
+//   the same, 16 new tokens (128 rows): V2 88.6 / 74.2 / 61.1 / 81.4
+//   64 seqs, lognormal lengths <= 32768, 16 new tokens (128 rows):
+//     253.7 / 354.3 / 279.4 / 250.6 / 254.1
+// More rows (chunked prefill): V1 when the V1 grid (num_seqs * num_kv_heads
+// CTAs per row split) gives every SM a CTA, else V2 at the caller's
+// partition size; its partials grow with the rows (chunked prefill, 2 x
+// 2048 new tokens after 30K: V1 2384 vs V2 4867 us at 512 tokens).
+// Fewer rows (the mma.sync kernel): V2 at the caller's partition size (8
+// rows: V2 92 vs V1 100 us; 16 rows: 99 vs 109).
+constexpr int kTcV2Partition = 2048;
+constexpr int kTcV2MaxRows = kTcRows;
+
 int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int head_dim,
-                      int max_seq_len, int partition_size, int sms)
+                      int max_seq_len, int partition_size, int sms, int *part_out)
 {
+    *part_out = partition_size;
     if (pa_v2_num_partitions(max_seq_len, partition_size) <= 1)
         return 1;
     const int cols = q_len * group;
-    // Counted with one query tile per CTA (the bf16 choice; fp16 may pair
-    // tiles, which happens only for many-row steps that fill the GPU anyway).
-    const long long ctas =
+    if (!use_tc(cols))
+        return 2;
+    // CTAs per partition index (one query tile per CTA: the bf16 choice; fp16
+    // may pair tiles, which happens only for many-row steps).
+    const long long per_part =
         (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim, PA_BF16, max_seq_len);
-    return (cols >= kTcMinRows && ctas >= sms) ? 1 : 2;
+    if (cols <= kTcV2MaxRows) {
+        int pc = partition_size > kTcV2Partition ? partition_size : kTcV2Partition;
+        while (pc / 2 >= partition_size &&
+               per_part * pa_v2_num_partitions(max_seq_len, pc) < sms)
+            pc /= 2;
+        if (pa_v2_num_partitions(max_seq_len, pc) <= 1)
+            return 1;
+        *part_out = pc;
+        return 2;
+    }
+    return per_part >= sms ? 1 : 2;
 }
 
 } // namespace
@@ -765,8 +796,27 @@ PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_k
     const int sms = sm_count(dev);
     if (sms <= 0)
         return -PA_ERR_CUDA;
+    int part = 0;
     return choose_variant_mq(num_seqs, q_len, num_heads / num_kv_heads, num_kv_heads, head_dim,
-                             max_seq_len, partition_size, sms);
+                             max_seq_len, partition_size, sms, &part);
+}
+
+PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int num_kv_heads,
+                                  int head_dim, int max_seq_len, int partition_size)
+{
+    if (num_seqs <= 0 || q_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || max_seq_len < 0 || partition_size <= 0)
+        return -PA_ERR_INVALID_ARG;
+    int dev;
+    if (current_device(&dev))
+        return -PA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return -PA_ERR_CUDA;
+    int part = 0;
+    const int v = choose_variant_mq(num_seqs, q_len, num_heads / num_kv_heads, num_kv_heads,
+                                    head_dim, max_seq_len, partition_size, sms, &part);
+    return v == 2 ? part : 0;
 }
 
 PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
@@ -792,6 +842,11 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
         pa_decode_mq_choose(num_seqs, q_len, num_heads, num_kv_heads, head_dim, cap, partition_size);
     if (which < 0)
         return -which;
+    const int part = which == 2 ? pa_decode_mq_partition(num_seqs, q_len, num_heads, num_kv_heads,
+                                                         head_dim, cap, partition_size)
+                                : partition_size;
+    if (part < 0)
+        return -part;
     if (which == 1)
         return pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                                q_len, num_heads, num_kv_heads, head_dim, num_blocks, block_size,
@@ -799,7 +854,7 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
                                stream);
     return pa_decode_v2_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                           max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype, out,
+                           max_blocks_per_seq, max_seq_len_hint, scale, part, dtype, out,
                            tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
 }
 

@@ -10,21 +10,40 @@
 // most 128 dims, and smaller (down to 16) when there are few (seq, head)
 // pairs.  A group of lanes owns one partition at a time and reads the
 // slice as float4s (contiguous bytes); the groups of a CTA take partitions
-// round robin and their running states meet in shared memory.
+// round robin, and their running states meet by warp shuffles and then in
+// shared memory.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 
-template <typename T, int DD>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams p)
+// Folds the running state (mo, lo, ao) into (m, l, a): the same
+// exp(m_old - M) rule as the partitions' own merge; a state with m = -inf
+// (no partition seen) adds nothing.
+__device__ __forceinline__ void merge_state(float &m, float &l, float4 &a, float mo, float lo,
+                                            float4 ao)
+{
+    const float M = fmaxf(m, mo);
+    const float f = m == -INFINITY ? 0.f : fast_exp2((m - M) * kLog2e);
+    const float g = mo == -INFINITY ? 0.f : fast_exp2((mo - M) * kLog2e);
+    l = fmaf(l, f, lo * g);
+    a.x = fmaf(a.x, f, ao.x * g);
+    a.y = fmaf(a.y, f, ao.y * g);
+    a.z = fmaf(a.z, f, ao.z * g);
+    a.w = fmaf(a.w, f, ao.w * g);
+    m = M;
+}
+
+template <typename T, int DD, int NTH>
+__global__ void __launch_bounds__(NTH) merge_kernel(const MergeParams p)
 {
     using E = Elem<T>;
-    constexpr int kGroup = DD / 4;                 // lanes per partition (one float4 each)
-    constexpr int kSlots = kMergeThreads / kGroup; // partitions in flight per CTA
-    __shared__ float s_m[kSlots];
-    __shared__ float s_l[kSlots];
-    __shared__ float4 s_acc[kSlots][kGroup];
+    constexpr int kGroup = DD / 4;         // lanes per partition (one float4 each)
+    constexpr int kSlots = NTH / kGroup;   // partitions in flight per CTA
+    constexpr int kWarps = NTH / 32;
+    __shared__ float s_m[kWarps][kGroup];
+    __shared__ float s_l[kWarps][kGroup];
+    __shared__ float4 s_acc[kWarps][kGroup];
 
     const int h = blockIdx.x;
     const int row = blockIdx.y;       // (sequence, new token) = b * q_len + i
@@ -33,6 +52,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
     const int d0 = blockIdx.z * DD;
     const int slot = threadIdx.x / kGroup; // partitions slot, slot + kSlots, ...
     const int c = threadIdx.x % kGroup;    // float4 column within the CTA's dims
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
 
     // The next call's attention grid may be scheduled while this one runs; it
     // waits for this grid's completion before it touches global memory.
@@ -78,28 +99,38 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeParams 
         l = fmaf(l, a, w);
         m = mn;
     }
-    s_acc[slot][c] = acc;
-    if (c == 0) {
-        s_m[slot] = m;
-        s_l[slot] = l;
+    // The slots of one warp (lanes with the same column c) meet by shuffles,
+    // then the warps meet in shared memory.
+#pragma unroll
+    for (int off = kGroup; off < 32; off <<= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+        const float lo = __shfl_xor_sync(0xffffffffu, l, off);
+        float4 ao;
+        ao.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+        ao.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+        ao.z = __shfl_xor_sync(0xffffffffu, acc.z, off);
+        ao.w = __shfl_xor_sync(0xffffffffu, acc.w, off);
+        merge_state(m, l, acc, mo, lo, ao);
+    }
+    if (lane < kGroup) {
+        s_m[warp][c] = m;
+        s_l[warp][c] = l;
+        s_acc[warp][c] = acc;
     }
     __syncthreads();
 
-    if (threadIdx.x < DD) {
-        const int d = threadIdx.x;
-        float M = -INFINITY;
+    if (threadIdx.x < kGroup) {
+        float M = s_m[0][c], tot = s_l[0][c];
+        float4 o = s_acc[0][c];
 #pragma unroll
-        for (int s = 0; s < kSlots; ++s)
-            M = fmaxf(M, s_m[s]);
-        float total = 0.f, o = 0.f;
-#pragma unroll
-        for (int s = 0; s < kSlots; ++s) {
-            const float f = s_m[s] == -INFINITY ? 0.f : fast_exp2((s_m[s] - M) * kLog2e);
-            total = fmaf(f, s_l[s], total);
-            const float *a = reinterpret_cast<const float *>(&s_acc[s][d >> 2]);
-            o = fmaf(f, a[d & 3], o);
-        }
-        out[d] = E::from_float(total > 0.f ? o / total : 0.f); // 0: the query sees no token
+        for (int w = 1; w < kWarps; ++w)
+            merge_state(M, tot, o, s_m[w][c], s_l[w][c], s_acc[w][c]);
+        const float inv = tot > 0.f ? 1.f / tot : 0.f; // 0: the query sees no token
+        T *o4 = out + 4 * c;
+        o4[0] = E::from_float(o.x * inv);
+        o4[1] = E::from_float(o.y * inv);
+        o4[2] = E::from_float(o.z * inv);
+        o4[3] = E::from_float(o.w * inv);
     }
 }
 
@@ -107,23 +138,39 @@ template <typename T>
 static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dd, const MergeParams &p)
 {
     switch (dd) {
-    case 16: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 16>, p);
-    case 32: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 32>, p);
-    case 64: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 64>, p);
-    default: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 128>, p);
+    case 16: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 16, kMergeThreads>, p);
+    case 32: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 32, kMergeThreads>, p);
+    case 64: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 64, kMergeThreads>, p);
+    default: return cudaLaunchKernelEx(&cfg, merge_kernel<T, 128, kMergeThreads>, p);
     }
 }
 
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
                          cudaStream_t stream)
 {
-    // A CTA owns at most 128 dims of head_dim; split further (down to 16
-    // dims) while the grid has fewer than about two CTAs per SM -- a finer
-    // split only adds CTAs of very little work.
+    // A CTA owns at most 128 dims of head_dim (dd); split further, down to 16
+    // dims, (a) while the grid has fewer than about two CTAs per SM, or (b)
+    // while the longest sequence has more partitions than one unrolled round
+    // of 4 per slot covers (slots = 128 threads / (dd / 4) lanes) and the
+    // grid stays within 16 CTAs per SM.  The CTA stays at 128 threads, so
+    // that these CTAs fit beside the attention kernel's (their registers come
+    // from what that kernel leaves free) and wait, already resident, for it
+    // to finish.  Measured on GB300 (us the merge adds to a call, same box):
+    // 8 x 131072 tokens at 1024 per partition (128 partitions): 7.3-8.5 at
+    // 128 dims per CTA; 256- and 512-thread CTAs cost the 100K-token and
+    // ragged batches 1.3 and 2.5 us instead, from not fitting beside the
+    // attention kernel.
     const long long pairs = (long long)p.num_heads * num_seqs * p.q_len;
+    const int np_max = (p.seq_len_cap + p.partition_size - 1) / p.partition_size;
     int dd = p.head_dim < 128 ? p.head_dim : 128;
-    while (dd > 16 && pairs * (p.head_dim / dd) < 2LL * num_sms)
-        dd /= 2;
+    while (dd > 16) {
+        const long long ctas = pairs * (p.head_dim / dd);
+        const int slots = kMergeThreads / (dd / 4);
+        if (ctas < 2LL * num_sms || (np_max > 4 * slots && 2 * ctas <= 16LL * num_sms))
+            dd /= 2;
+        else
+            break;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.num_heads, num_seqs * p.q_len, p.head_dim / dd);
     cfg.blockDim = dim3(kMergeThreads);

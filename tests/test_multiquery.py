@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as wl
-from parity_util import check_mq, mq, run_mq
+from parity_util import check_mq, check_out, mq, run_mq
 
 pytestmark = pytest.mark.gpu
 
@@ -63,26 +63,42 @@ def test_mq_partition_not_a_multiple_of_block_size(q_len, G, bs, P):
 
 
 def test_mq_dispatch_rule_and_entry(cuda_lib):
-    """pa_decode_mq runs the variant pa_decode_mq_choose names (bitwise the same output)."""
+    """pa_decode_mq runs the variant pa_decode_mq_choose names, at the partition size
+    pa_decode_mq_partition names (bitwise the same output as that entry point)."""
     import paged_kv_decode_v2_gb300 as pa
     # batch decode shapes (32 seqs, 32 / 8 heads, up to 8192 tokens, P = 512)
     assert pa.pa_decode_mq_choose(32, 2, 32, 8, 128, 8192, 512) == 2   # 8 rows per KV head
     assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 8192, 512) == 2   # 16 rows (mma.sync)
-    assert pa.pa_decode_mq_choose(32, 8, 32, 8, 128, 8192, 512) == 1   # 32 rows (tcgen05), 256 CTAs
-    assert pa.pa_decode_mq_choose(32, 32, 32, 8, 128, 8192, 512) == 1
+    assert pa.pa_decode_mq_partition(32, 4, 32, 8, 128, 8192, 512) == 512
+    for q in (8, 16, 32):                                                # 32..128 rows (tcgen05)
+        assert pa.pa_decode_mq_choose(32, q, 32, 8, 128, 8192, 512) == 2
+        assert pa.pa_decode_mq_partition(32, q, 32, 8, 128, 8192, 512) == 2048
+    assert pa.pa_decode_mq_partition(32, 16, 32, 8, 128, 8192, 4096) == 4096
+    assert pa.pa_decode_mq_choose(32, 16, 32, 8, 128, 2048, 512) == 1   # one 2048 partition
+    assert pa.pa_decode_mq_partition(32, 16, 32, 8, 128, 2048, 512) == 0
+    assert pa.pa_decode_mq_choose(32, 64, 32, 8, 128, 8192, 512) == 1  # 256 rows: V1
     assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 100000, 512) == 2  # one long sequence
+    assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 100000, 512) == 2048
+    assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 20000, 512) == 512  # 160 CTAs at 512
     assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 512, 512) == 1     # one partition
-    w = mq("mq_dispatch", 4, 4, (3, 100, 700, 1500), P=256, seed=79)
-    inp = wl.make_inputs(w, device="cuda")
-    S, Q, H, D = inp.query.shape
-    want = pa.pa_decode_mq_choose(S, Q, H, w.num_kv_heads, D, inp.block_tables.shape[1] * w.block_size, 256)
-    ref = run_mq(inp, 256, entry="v1" if want == 1 else "v2")[0]
-    tmp, es, ml = pa.alloc_workspace(S, H, D, pa.num_partitions(inp.block_tables.shape[1] * w.block_size, 256), q_len=Q)
-    out = torch.full_like(inp.query, float("nan"))
-    pa.pa_decode_mq(inp.query, inp.key_cache, inp.value_cache, inp.block_tables, inp.seq_lens, w.scale,
-                    256, out, tmp, es, ml)
-    torch.cuda.synchronize()
-    assert torch.equal(out, ref)
+    for (q_len, G, lens, P) in ((4, 4, (3, 100, 700, 1500), 256),
+                                (16, 4, (3, 100, 2500, 6000, 777), 256)):
+        w = mq("mq_dispatch", q_len, G, lens, P=P, seed=79 + q_len)
+        inp = wl.make_inputs(w, device="cuda")
+        S, Q, H, D = inp.query.shape
+        cap = inp.block_tables.shape[1] * w.block_size
+        want = pa.pa_decode_mq_choose(S, Q, H, w.num_kv_heads, D, cap, P)
+        part = pa.pa_decode_mq_partition(S, Q, H, w.num_kv_heads, D, cap, P)
+        assert (want == 1) == (part == 0)
+        ref = run_mq(inp, part if want == 2 else P, entry="v1" if want == 1 else "v2")[0]
+        tmp, es, ml = pa.alloc_workspace(S, H, D, pa.num_partitions(cap, P), q_len=Q)
+        out = torch.full_like(inp.query, float("nan"))
+        pa.pa_decode_mq(inp.query, inp.key_cache, inp.value_cache, inp.block_tables,
+                        inp.seq_lens, w.scale, P, out, tmp, es, ml)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+        check_out(out, oracle.decode(oracle.Problem.from_arrays(wl.to_oracle_arrays(inp))),
+                  w.dtype, what=f"mq_dispatch q{q_len}")
 
 
 def test_mq_single_token_matches_the_single_query_entry():
