@@ -416,7 +416,10 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 float x[kTcTok];
                 float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY}; // independent chains
                 float mx, cf;
-                if (__all_sync(0xffffffffu, scale > 0.f && off >= 0 && off + kTcTok <= (int)span)) {
+                // Padding rows of a partly filled warp vote yes: their P reaches only
+                // O rows that are never stored.
+                if (__all_sync(0xffffffffu,
+                               !row_ok || (scale > 0.f && off >= 0 && off + kTcTok <= (int)span))) {
 #pragma unroll
                     for (int c = 0; c < kTcTok; ++c) {
                         x[c] = __uint_as_float(sr[c >> 5][c & 31]);
@@ -438,13 +441,13 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 // Move m when a row of the warp would otherwise see P > 2^8 (the
                 // first visible tile always: m_run = -inf).  NaN (both -inf) is no.
                 float a = 1.f;
-                if (__any_sync(0xffffffffu, (mx - m_run) * kLog2e > kTcRescaleLog2)) {
+                if (__any_sync(0xffffffffu, row_ok && (mx - m_run) * kLog2e > kTcRescaleLog2)) {
                     const float mn = fmaxf(m_run, mx);
                     // A row with no visible token yet (max still -inf) keeps l = o = 0.
                     a = mn != -INFINITY ? fast_exp2((m_run - mn) * kLog2e) : 1.f;
                     m_run = mn;
                     // O is rescaled once the last P.V has landed (tile 0 has no O yet).
-                    if (t > 0 && __any_sync(0xffffffffu, a != 1.f)) {
+                    if (t > 0 && __any_sync(0xffffffffu, row_ok && a != 1.f)) {
                         if (!__all_sync(0xffffffffu,
                                         mbar_wait_abortable(b_o_done + 8 * ((t - 1) & 1),
                                                             (uint32_t)((t - 1) >> 1) & 1u, abort_flag))) {
