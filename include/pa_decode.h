@@ -341,7 +341,10 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
  * the one-tile tcgen05 kernel; 4 always the two-tile one (one tile for
  * head_dim 256); 5 the CUDA-core kernel (Q.K and the softmax reduced with
  * warp shuffles, P.V as scalar FMAs, no tensor-core instruction) up to 8
- * rows, else as 0.  Either kernel computes the same
+ * rows, else as 0; 6 always the one-tile tcgen05 kernel with its whole
+ * 128-row Q tile stored (by default a KV head of at most 64 rows stores only
+ * the 64 rows it uses and spends the space on a deeper ring).  Either kernel
+ * computes the same
  * result within the stated tolerances; the choice changes only speed.  The
  * tcgen05 kernel takes its K ring stages from pa_set_launch_config's
  * stages_per_warp and its V ring stages from warps_per_cta when those are

@@ -304,7 +304,8 @@ def pa_set_launch_config(warps_per_cta: int = 0, stages_per_warp: int = 0) -> No
 def pa_set_rows_kernel(mode: int = 0) -> None:
     """0: by query rows per KV head; 1: always mma.sync; 2: always tcgen05; 3: tcgen05, one
     query tile per CTA; 4: tcgen05, two query tiles per CTA; 5: the CUDA-core (SIMT) kernel
-    up to 8 rows per KV head, else as 0."""
+    up to 8 rows per KV head, else as 0; 6: tcgen05, one query tile per CTA with the whole
+    128-row Q tile stored (modes 0 and 3 store 64 rows for KV heads of at most 64 rows)."""
     _check("pa_set_rows_kernel", load().pa_set_rows_kernel(mode))
 
 

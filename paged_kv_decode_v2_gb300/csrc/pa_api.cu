@@ -21,7 +21,8 @@ std::atomic<int> g_tune_stages{0};
 // Kernel for the query rows of a KV head: 0 = by row count, 1 = always the
 // mma.sync kernel, 2 = always a tcgen05 kernel (query tiles by row count),
 // 3 = the one-tile tcgen05 kernel, 4 = the two-tile one (head_dim <= 128),
-// 5 = the CUDA-core (SIMT) kernel up to 8 rows, else as 0.
+// 5 = the CUDA-core (SIMT) kernel up to 8 rows, else as 0, 6 = the one-tile
+// tcgen05 kernel with the whole 128-row Q tile stored at every row count.
 std::atomic<int> g_rows_kernel{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
@@ -300,10 +301,13 @@ int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles)
 
 // The tcgen05 kernels.  One query tile: as many K and V ring stages as keep
 // two CTAs per SM for head_dim <= 128 (one for 256 dims, whose TMEM takes
-// the whole SM).  Two query tiles (one CTA per SM, all 512 TMEM columns):
-// 2 + 2 stages of 128 tokens at head_dim 128, 4 + 4 at 64.
-// pa_set_launch_config's stages_per_warp overrides the K stages and its
-// warps_per_cta the V stages.
+// the whole SM): 2 + 2 stages of 64 tokens at head_dim 128, 4 + 4 at 64.  A
+// KV head of at most 64 rows stores only the 64 Q rows it uses (half Q
+// tile), and at head_dim 128 the 16 KB saved hold a third V stage.  Two
+// query tiles (one CTA per SM, all 512 TMEM columns): 2 + 2 stages of 128
+// tokens at head_dim 128, 4 + 4 at 64.  pa_set_launch_config's
+// stages_per_warp overrides the K stages and its warps_per_cta the V
+// stages.
 int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
 {
     const int tiles = L.tc_tiles;
@@ -318,12 +322,16 @@ int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
             return PA_ERR_CUDA;
         g_tc_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
     }
+    const bool q_half = L.p.q_half != 0;
     auto bytes = [&](int ks, int vs) {
-        return tiles == 2 ? tc2_smem_bytes(L.head_dim, ks, vs) : tc_smem_bytes(L.head_dim, ks, vs);
+        return tiles == 2 ? tc2_smem_bytes(L.head_dim, ks, vs)
+                          : tc_smem_bytes(L.head_dim, ks, vs, q_half);
     };
     const int tune_s = g_tune_stages.load(std::memory_order_relaxed);
     const int tune_w = g_tune_warps.load(std::memory_order_relaxed);
     int ks = L.head_dim == 64 ? 4 : 2, vs = ks;
+    if (q_half && L.head_dim == 128)
+        vs = 3;
     if (tune_s > 0)
         ks = tune_s;
     if (tune_w > 0)
@@ -367,7 +375,7 @@ int prepare_and_launch_attn(AttnLaunch &L, cudaStream_t stream)
 bool use_tc(int cols)
 {
     const int mode = g_rows_kernel.load(std::memory_order_relaxed);
-    if (mode >= 2 && mode <= 4)
+    if ((mode >= 2 && mode <= 4) || mode == 6)
         return true;
     return (mode == 0 || mode == 5) && cols >= kTcMinRows;
 }
@@ -384,7 +392,7 @@ bool use_tc(int cols)
 int tc_tiles(int cols, int head_dim, int dtype, int max_seq_len)
 {
     const int mode = g_rows_kernel.load(std::memory_order_relaxed);
-    if (head_dim > 128 || mode == 3)
+    if (head_dim > 128 || mode == 3 || mode == 6)
         return 1;
     if (mode == 4)
         return 2;
@@ -436,6 +444,11 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
         // 128 rows per query tile; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
         L.tc_tiles = tc_tiles(p.cols, head_dim, dtype, cap);
+        // At most 64 rows on one tile: only Q rows 64-127 are stored.
+        p.q_half = (L.tc_tiles == 1 && p.cols <= kTcRows / 2 &&
+                    g_rows_kernel.load(std::memory_order_relaxed) != 6)
+                       ? 1
+                       : 0;
         p.col_groups = row_ctas(p.cols, head_dim, dtype, cap);
     } else {
         // Up to 8 query rows: one n-tile (or the SIMT kernel when asked for);
@@ -912,7 +925,7 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp)
 
 PA_API int pa_set_rows_kernel(int mode)
 {
-    if (mode < 0 || mode > 5)
+    if (mode < 0 || mode > 6)
         return PA_ERR_INVALID_ARG;
     g_rows_kernel.store(mode, std::memory_order_relaxed);
     return PA_OK;

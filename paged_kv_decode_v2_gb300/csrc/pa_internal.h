@@ -41,6 +41,7 @@ struct AttnParams {
     int partition_size;          // V2: tokens per partition (any positive value)
     int stages;                  // TMA ring stages per warp (tcgen05 kernel: K ring stages)
     int v_stages;                // tcgen05 kernel: V ring stages
+    int q_half;                  // tcgen05 one-tile kernel: only Q rows 64-127 stored (<= 64 rows)
     int max_num_partitions;      // V2: partition capacity of the intermediates
     float *tmp_output;           // V2: [S, q_len, H, NPcap, D]
     float *exp_sums;             // V2: [S, q_len, H, NPcap]
@@ -145,9 +146,9 @@ inline const AttnOps *simt_ops(int dtype, int head_dim)
 // Dynamic shared memory of the tcgen05 kernel: the Q tile, k_stages K tiles
 // and v_stages V tiles, and 1 KB to align the base to the 1024-byte swizzle
 // atom.
-inline size_t tc_smem_bytes(int head_dim, int k_stages, int v_stages)
+inline size_t tc_smem_bytes(int head_dim, int k_stages, int v_stages, bool q_half = false)
 {
-    return 1024 + (size_t)kTcRows * head_dim * 2 +
+    return 1024 + (size_t)(q_half ? kTcRows / 2 : kTcRows) * head_dim * 2 +
            (size_t)(k_stages + v_stages) * kTcTok * head_dim * 2;
 }
 

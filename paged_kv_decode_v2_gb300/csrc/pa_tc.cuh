@@ -32,6 +32,14 @@
 // on which m was used.  The true max is tracked beside it, and a V2 partial
 // reports that max with l rescaled to it, as the merge expects.
 //
+// Half Q tile (p.q_half, a KV head of at most 64 rows): the rows sit at M
+// indices 64-127, so only those 64 rows of Q are stored, 8 KB per 64-dim
+// slice instead of 16.  The S MMA still reads 128 rows: its descriptor
+// starts 8 KB before each stored slice, so the padding rows 0-63 read
+// whatever lies there (the end of the K ring, or the previous slice).  MMA
+// rows are independent and those rows' S, P and O are never stored, so the
+// saved 16 KB (head_dim 128) buy a third ring stage at two CTAs per SM.
+//
 // Warp roles: warps 0-3 own the 128 rows (softmax, epilogue), warp 4 issues
 // the MMAs (one thread) and owns the TMEM allocation, two lanes of warp 5
 // gather the K and the V blocks of each 64-token tile with TMA, each into its
@@ -167,9 +175,14 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     const int kst = p.stages;   // K ring stages
     const int vst = p.v_stages; // V ring stages
     const uint32_t smem0 = (smem_addr(dyn_smem) + 1023u) & ~1023u;
-    const uint32_t q_sm = smem0;
-    const uint32_t k_sm = smem0 + C::kQBytes;
-    const uint32_t v_sm = k_sm + (uint32_t)kst * C::kKVBytes;
+    // Layout: [Q | K ring | V ring], or with a half Q tile [K ring | Q | V
+    // ring], the K ring then holding the 8 KB the first slice's padding rows
+    // alias (kst >= 1 K stages of >= 8 KB each).
+    const bool q_half = p.q_half != 0;
+    const uint32_t q_slice = q_half ? C::kQSlice / 2 : C::kQSlice; // bytes between Q slices
+    const uint32_t k_sm = q_half ? smem0 : smem0 + C::kQBytes;
+    const uint32_t q_sm = q_half ? k_sm + (uint32_t)kst * C::kKVBytes : smem0;
+    const uint32_t v_sm = q_half ? q_sm + C::kQBytes / 2 : k_sm + (uint32_t)kst * C::kKVBytes;
     const uint32_t b_k_full = smem_addr(k_full), b_v_full = smem_addr(v_full);
     const uint32_t b_k_empty = smem_addr(k_empty), b_v_empty = smem_addr(v_empty);
     const uint32_t b_q_full = smem_addr(&q_full), b_s_full = smem_addr(s_full);
@@ -289,7 +302,9 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
             constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
             // Descriptors are linear in the address (start / 16 in the low
             // bits, shared memory < 256 KB): offsets are added to a base.
-            const uint64_t qd = smem_desc_sw128(q_sm, 16, 1024);
+            // With a half Q tile, each slice's descriptor starts 64 rows (8 KB)
+            // before its stored rows 64-127.
+            const uint64_t qd = smem_desc_sw128(q_half ? q_sm - C::kQSlice / 2 : q_sm, 16, 1024);
             const uint64_t kd = smem_desc_sw128(k_sm, 16, 1024);
             const uint64_t vd = smem_desc_sw128(v_sm, C::kKVSlice, 1024);
             int ks_next = 0;       // K ring stage of the next S
@@ -303,7 +318,7 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
                 const uint64_t kb = kd + (((uint32_t)ks_next * C::kKVBytes) >> 4);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off_q = (ks >> 2) * C::kQSlice + (ks & 3) * 32;
+                    const uint32_t off_q = (ks >> 2) * q_slice + (ks & 3) * 32;
                     const uint32_t off_k = (ks >> 2) * C::kKVSlice + (ks & 3) * 32;
                     tc_mma_ss(sc, qd + (off_q >> 4), kb + (off_k >> 4), idesc_s, ks > 0);
                 }
@@ -357,20 +372,22 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     } else {
         // ---------------------------------------------------------- rows
         // Q row -> shared memory, 128-byte swizzled (16-byte chunk c of a row
-        // of 64 dims at (c ^ (row & 7)) * 16), zero for padding rows.
-        {
+        // of 64 dims at (c ^ (row & 7)) * 16), zero for padding rows; with a
+        // half Q tile only rows 64-127 are stored, at row - 64.
+        if (!q_half || r >= kTcRows / 2) {
+            const int qr = q_half ? r - kTcRows / 2 : r;
 #pragma unroll
             for (int ch = 0; ch < kQChunks; ++ch) {
                 const uint4 v = ch < kEarly ? q_early[ch] : q_chunk(ch);
                 const uint32_t addr =
-                    q_sm + (ch >> 3) * C::kQSlice + r * 128 + ((((ch & 7) ^ (r & 7))) << 4);
+                    q_sm + (ch >> 3) * q_slice + qr * 128 + ((((ch & 7) ^ (r & 7))) << 4);
                 asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x),
                              "r"(v.y), "r"(v.z), "r"(v.w)
                              : "memory");
             }
-            fence_proxy_async();
-            mbar_arrive(b_q_full);
         }
+        fence_proxy_async();
+        mbar_arrive(b_q_full);
         if (warp * 32 + 32 <= roff) {
             // A warp of padding rows only: one arrival on "P ready" per tile,
             // after that tile's S, keeps the barrier's count (never a phase

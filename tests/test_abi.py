@@ -133,7 +133,8 @@ def test_multi_query_dispatch_validation(cuda_lib):
 def test_rows_kernel_override_validation(cuda_lib):
     lib = cuda_lib.load()
     assert lib.pa_set_rows_kernel(-1) == 1
-    assert lib.pa_set_rows_kernel(6) == 1
+    assert lib.pa_set_rows_kernel(7) == 1
+    assert lib.pa_set_rows_kernel(6) == 0
     assert lib.pa_set_rows_kernel(5) == 0
     assert lib.pa_set_rows_kernel(4) == 0
     assert lib.pa_set_rows_kernel(2) == 0

@@ -2,8 +2,10 @@
 the GQA group) per CTA, S = Q K^T and O += P V on the fifth-generation
 tensor cores with S, P and O in tensor memory.
 
-Every test forces each of the two tcgen05 kernels in turn (one or two 128-row
-query tiles per CTA; pa_set_rows_kernel 3 and 4) and compares the CUDA path,
+Every test forces each tcgen05 kernel form in turn (one 128-row query tile per
+CTA, storing only 64 Q rows for KV heads of at most 64 rows; the same with the
+whole Q tile stored; two tiles per CTA; pa_set_rows_kernel 3, 6 and 4) and
+compares the CUDA path,
 V2 (partials + merge) and V1, element by element with the fp64 oracle,
 with the tolerances of parity_util: row counts below, at and above one CTA's
 128 rows, every head_dim and block size, K/V tiles that end inside a block,
@@ -22,10 +24,11 @@ from parity_util import (check_mq, check_out, check_partitions, mq, oracle_probl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=[3, 4], ids=["one_tile", "two_tiles"])
+@pytest.fixture(autouse=True, params=[3, 6, 4], ids=["one_tile", "one_tile_full_q", "two_tiles"])
 def _force_tc(request, cuda_lib):
-    """Each test runs with the one-tile kernel (128 query rows per CTA) and with
-    the two-tile kernel (two 128-row tiles sharing each 128-token K/V tile;
+    """Each test runs with the one-tile kernel (128 query rows per CTA; at most 64 rows store
+    only their half of the Q tile), the one-tile kernel with the whole Q tile stored at every
+    row count, and the two-tile kernel (two 128-row tiles sharing each 128-token K/V tile;
     head_dim 256 stays on one tile)."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
