@@ -168,9 +168,11 @@ PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *va
  * The other arguments are pa_decode_v2's; tmp_output, exp_sums and
  * max_logits hold the partials afterwards exactly as after pa_decode_v2.
  * Runs on the mma.sync kernel whatever the group size (no tcgen05 or SIMT
- * variant).  Measured against pa_decode_v2 on this GPU it is slower on the
- * decode workloads (see the project's design notes), so pa_decode never
- * picks it; it is a separate entry point.
+ * variant).  Measured against pa_decode_v2 on GB300 it is faster only when
+ * the merge is trivial and the call latency-bound (one 1000-token sequence:
+ * 10.4 vs 11.3 us) and slower otherwise, most of all with many partitions,
+ * whose merge then runs on one CTA (one 100K-token sequence at 512 tokens
+ * per partition: 97.5 vs 38.0 us); pa_decode never picks it.
  */
 PA_API int pa_decode_v2_fused(const void *query, const void *key_cache, const void *value_cache,
                               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,
