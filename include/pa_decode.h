@@ -28,8 +28,8 @@
  * walks every block with a running {m, l, o}; "vllm/_custom_ops.py" commit
  * 900ae0b, "V1: 1 CTA iterates ... partitions sequentially").  pa_decode
  * chooses between them ("paged_attn.py" commit 490ff98, change 1: restore
- * the V1/V2 adaptive dispatch), with a rule re-measured on this GPU: V1
- * when the longest sequence fits one partition, else V2.
+ * the V1/V2 adaptive dispatch), with a rule re-measured on this GPU (see
+ * pa_decode_choose).
  *
  * Layouts (all row-major, contiguous, device memory)
  * --------------------------------------------------
@@ -300,13 +300,14 @@ PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *va
 /*
  * Which variant pa_decode runs for these sizes on the current device:
  * returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.  Host only.
- * The rule: V1 when ceil(max_seq_len / partition_size) <= 1 (a merge of one
- * partition would only copy), else V2.  num_seqs and num_kv_heads are
- * validated (> 0) but are reserved: they do not change the answer.  A
- * grid-fill rule (V1 once num_seqs * num_kv_heads CTAs fill the device) was
- * measured on this GPU and lost to V2 in every regime with more than one
- * partition (512 sequences of <= 1024 tokens: V2 177 us, V1 196 us), so the
- * two counts are kept in the signature for a future rule and ignored now.
+ * The rule, measured on GB300 ("paged_attn.py" commit 490ff98, change 1,
+ * restores a V1/V2 dispatch; its 8192-token switch point was set on other
+ * hardware): with NP = ceil(max_seq_len / partition_size),
+ *   V1 if NP <= 1 (a merge of one partition would only copy), or if NP == 2
+ *      and num_seqs * num_kv_heads (V1's CTAs) is at most the number of SMs
+ *      (a latency-bound call, where the merge's second launch costs more
+ *      than splitting each sequence in two);
+ *   V2 otherwise.
  */
 PA_API int pa_decode_choose(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size);
 

@@ -578,16 +578,21 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
 
 int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size, int sms)
 {
-    // num_seqs, num_kv_heads and the SM count are reserved (the header says
-    // so): a grid-fill rule built on them lost to the rule below.
-    (void)num_seqs;
-    (void)num_kv_heads;
-    (void)sms;
-    // One partition: V2's merge would only copy, so V1.  Otherwise V2: on
-    // GB300 it matched or beat V1 in every measured regime, including many
-    // short sequences (256 x <=1536 tokens: 134.5 vs 135.2 us; 512 x <=1024:
-    // 177.4 vs 195.8 us; batch decode: 85.2 vs 97.2 us).
-    return pa_v2_num_partitions(max_seq_len, partition_size) <= 1 ? 1 : 2;
+    // One partition: V2's merge would only copy, so V1.  Two partitions and a
+    // V1 grid of at most one CTA per SM: the call is latency-bound and the
+    // merge's fixed cost (a second launch behind the first) outweighs
+    // splitting each sequence in two, so V1.  Otherwise V2.  Measured on
+    // GB300 (us, V1 vs V2, 32 / 8 or 8 / 2 heads, P = 512): 1 seq x 1000
+    // tokens 9.6 vs 10.6, 8 x 600 7.9 vs 10.9, 8 x 1000 10.4 vs 11.8; from
+    // three partitions V2 wins (1 x 1500: 12.7 vs 10.6; 4 x 2000: 16.2 vs
+    // 11.9), and with two partitions on a large grid too (512 x <= 1024:
+    // 195.8 vs 177.4; 32 seqs of U{1..8192}: 97.2 vs 85.2).
+    const int np = pa_v2_num_partitions(max_seq_len, partition_size);
+    if (np <= 1)
+        return 1;
+    if (np == 2 && (long long)num_seqs * num_kv_heads <= sms)
+        return 1;
+    return 2;
 }
 
 // Several new tokens per sequence: which variant pa_decode_mq runs, and with

@@ -212,10 +212,16 @@ def test_batch_decode_full_size_every_element():
 
 
 def test_dispatch_rule(cuda_lib):
-    """V1 when the longest sequence fits one partition, else V2."""
+    """V1 when the longest sequence fits one partition, or fits two and V1's grid (sequences x
+    KV heads) has at most one CTA per SM; else V2."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
     assert cuda_lib.pa_decode_choose(32, 8, 512, 512) == 1
     assert cuda_lib.pa_decode_choose(4096, 8, 300, 512) == 1
-    assert cuda_lib.pa_decode_choose(1, 4, 513, 512) == 2
+    assert cuda_lib.pa_decode_choose(1, 4, 513, 512) == 1          # two partitions, 4 CTAs
+    assert cuda_lib.pa_decode_choose(1, 2, 1000, 512) == 1         # the tiny workload
+    assert cuda_lib.pa_decode_choose(sms, 1, 1024, 512) == 1
+    assert cuda_lib.pa_decode_choose(sms + 1, 1, 1024, 512) == 2
+    assert cuda_lib.pa_decode_choose(1, 4, 1025, 512) == 2         # three partitions
     assert cuda_lib.pa_decode_choose(512, 8, 1024, 512) == 2
     assert cuda_lib.pa_decode_choose(1, 4, 100000, 1024) == 2
 
