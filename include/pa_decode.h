@@ -248,7 +248,10 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
  * current device: returns 1 (V1) or 2 (V2), or a negative PA_ERR_* code.
  * Host only.  With R = q_len * G query rows per KV head:
  *   - one partition covers max_seq_len: V1;
- *   - R < 32 (the mma.sync kernel): V2;
+ *   - R < 32 (the mma.sync kernel): V2, for q_len >= 2 at the partition
+ *     size pa_decode_mq_partition returns (1024 tokens unless
+ *     partition_size is larger or the grid would leave SMs idle; V1 when
+ *     that partition covers max_seq_len), for q_len = 1 at partition_size;
  *   - 32 <= R <= 128 (the tcgen05 kernel, one query tile): V2 at the
  *     partition size pa_decode_mq_partition returns (2048 tokens unless
  *     partition_size is larger, or the grid would leave SMs idle), or V1

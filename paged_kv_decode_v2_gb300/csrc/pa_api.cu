@@ -618,10 +618,16 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 // CTAs per row split) gives every SM a CTA, else V2 at the caller's
 // partition size; its partials grow with the rows (chunked prefill, 2 x
 // 2048 new tokens after 30K: V1 2384 vs V2 4867 us at 512 tokens).
-// Fewer rows (the mma.sync kernel): V2 at the caller's partition size (8
-// rows: V2 92 vs V1 100 us; 16 rows: 99 vs 109).
+// Fewer rows (the mma.sync kernel, 2 or more new tokens): V2 on partitions
+// of max(partition_size, 1024) tokens, halved the same way (us; V1 / V2 at
+// 512 / 1024 / 2048): batch decode, 2 new tokens (8 rows) 96.5 / 86.1 /
+// 86.6 / 122.8; 4 tokens (16 rows) 107.8 / 97.9 / 96.3 / 149.8; ragged, 2
+// tokens (16 rows) 157.1 / 139.4 / 119.3 / 118.8; the 100K-token sequence,
+// 2 tokens (16 rows) V2 44.2 / 41.1 / 42.9.  A single new token takes the
+// caller's partition size, as pa_decode does.
 constexpr int kTcV2Partition = 2048;
 constexpr int kTcV2MaxRows = kTcRows;
+constexpr int kMmaV2Partition = 1024;
 
 int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int head_dim,
                       int max_seq_len, int partition_size, int sms, int *part_out)
@@ -630,8 +636,20 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
     if (pa_v2_num_partitions(max_seq_len, partition_size) <= 1)
         return 1;
     const int cols = q_len * group;
-    if (!use_tc(cols))
+    if (!use_tc(cols)) {
+        if (q_len == 1)
+            return 2;
+        const long long per_part_mma = (long long)num_seqs * num_kv_heads *
+                                       row_ctas(cols, head_dim, PA_BF16, max_seq_len);
+        int pc = partition_size > kMmaV2Partition ? partition_size : kMmaV2Partition;
+        while (pc / 2 >= partition_size &&
+               per_part_mma * pa_v2_num_partitions(max_seq_len, pc) < sms)
+            pc /= 2;
+        if (pa_v2_num_partitions(max_seq_len, pc) <= 1)
+            return 1;
+        *part_out = pc;
         return 2;
+    }
     // CTAs per partition index (one query tile per CTA: the bf16 choice; fp16
     // may pair tiles, which happens only for many-row steps).
     const long long per_part =

@@ -69,7 +69,9 @@ def test_mq_dispatch_rule_and_entry(cuda_lib):
     # batch decode shapes (32 seqs, 32 / 8 heads, up to 8192 tokens, P = 512)
     assert pa.pa_decode_mq_choose(32, 2, 32, 8, 128, 8192, 512) == 2   # 8 rows per KV head
     assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 8192, 512) == 2   # 16 rows (mma.sync)
-    assert pa.pa_decode_mq_partition(32, 4, 32, 8, 128, 8192, 512) == 512
+    assert pa.pa_decode_mq_partition(32, 4, 32, 8, 128, 8192, 512) == 1024
+    assert pa.pa_decode_mq_partition(32, 1, 32, 8, 128, 8192, 512) == 512   # one new token
+    assert pa.pa_decode_mq_choose(32, 4, 32, 8, 128, 1024, 512) == 1   # one 1024 partition
     for q in (8, 16, 32):                                                # 32..128 rows (tcgen05)
         assert pa.pa_decode_mq_choose(32, q, 32, 8, 128, 8192, 512) == 2
         assert pa.pa_decode_mq_partition(32, q, 32, 8, 128, 8192, 512) == 2048
