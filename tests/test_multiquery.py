@@ -183,3 +183,22 @@ def test_mq_random_shapes_default_dispatch(case):
     q_len, G, D, bs, P, dtype, lens, seed = case
     w = mq("mq_random", q_len, G, lens, bs=bs, P=P, D=D, dtype=dtype, seed=seed)
     check_mq(wl.make_inputs(w, device="cuda"), P)
+
+
+@pytest.mark.parametrize("case", _random_mq_cases(12, 20261204), ids=lambda c: f"q{c[0]}g{c[1]}d{c[2]}b{c[3]}p{c[4]}")
+def test_mq_random_shapes_through_the_dispatch(case):
+    """Seeded random shapes through pa_decode_mq, whose V2 may run on partitions coarser than the
+    caller's (pa_decode_mq_partition), element by element against the oracle."""
+    import paged_kv_decode_v2_gb300 as pa
+    q_len, G, D, bs, P, dtype, lens, seed = case
+    w = mq("mq_dispatch_random", q_len, G, lens, bs=bs, P=P, D=D, dtype=dtype, seed=seed + 50)
+    inp = wl.make_inputs(w, device="cuda")
+    S, Q, H, Dh = inp.query.shape
+    cap = inp.block_tables.shape[1] * w.block_size
+    tmp, es, ml = pa.alloc_workspace(S, H, Dh, max(1, pa.num_partitions(cap, P)), q_len=Q)
+    out = torch.full_like(inp.query, float("nan"))
+    pa.pa_decode_mq(inp.query, inp.key_cache, inp.value_cache, inp.block_tables, inp.seq_lens,
+                    w.scale, P, out, tmp, es, ml)
+    torch.cuda.synchronize()
+    check_out(out, oracle.decode(oracle.Problem.from_arrays(wl.to_oracle_arrays(inp))), dtype,
+              what="mq_dispatch_random")
