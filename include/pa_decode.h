@@ -252,11 +252,15 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
  *     size pa_decode_mq_partition returns (1024 tokens unless
  *     partition_size is larger or the grid would leave SMs idle; V1 when
  *     that partition covers max_seq_len), for q_len = 1 at partition_size;
- *   - 32 <= R <= 128 (the tcgen05 kernel, one query tile): V2 at the
- *     partition size pa_decode_mq_partition returns (2048 tokens unless
- *     partition_size is larger, or the grid would leave SMs idle), or V1
- *     when that partition covers max_seq_len;
- *   - R > 128 (chunked prefill): V1 when the V1 grid (num_seqs *
+ *   - R >= 32 (the tcgen05 kernels) and few (sequence, KV head, row tile)
+ *     groups, at most half the CTAs resident at once: V2 on partitions
+ *     sized so that the longest sequence's CTAs make one wave (a multiple
+ *     of 64 tokens, at least partition_size), V1 if one partition covers it;
+ *   - otherwise 32 <= R <= 128 (one query tile): V2 at the partition size
+ *     pa_decode_mq_partition returns (2048 tokens unless partition_size is
+ *     larger, or the grid would leave SMs idle), or V1 when that partition
+ *     covers max_seq_len;
+ *   - otherwise R > 128 (chunked prefill): V1 when the V1 grid (num_seqs *
  *     num_kv_heads CTAs per 128-row tile) gives every SM a CTA, else V2.
  * There is no counterpart in the method's description, which dispatches
  * single-token decode only; the rule is measured on GB300.
@@ -265,10 +269,9 @@ PA_API int pa_decode_mq_choose(int num_seqs, int q_len, int num_heads, int num_k
                                int head_dim, int max_seq_len, int partition_size);
 
 /*
- * The partition size pa_decode_mq runs V2 with for these sizes: a multiple
- * of partition_size by a power of two (at least partition_size; the
- * intermediates sized for partition_size therefore always suffice), or 0
- * when it runs V1.  Negative PA_ERR_* code for invalid arguments.  Host
+ * The partition size pa_decode_mq runs V2 with for these sizes: at least
+ * partition_size (the intermediates sized for partition_size therefore
+ * always suffice), or 0 when it runs V1.  Negative PA_ERR_* code for invalid arguments.  Host
  * only.  No counterpart in the method's description.
  */
 PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int num_kv_heads,

@@ -598,7 +598,16 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 // Several new tokens per sequence: which variant pa_decode_mq runs, and with
 // which partition size (*part_out) if V2.
 //
-// 32 to 128 query rows per KV head (the tcgen05 kernel, one 128-row tile):
+// The tcgen05 kernel with few (sequence, KV head, row tile) groups -- at
+// most half the CTAs that are resident at once -- runs V2 on partitions
+// sized so that the longest sequence's CTAs make exactly one wave (rounded
+// up to the 64-token tile, never finer than partition_size).  Measured on
+// GB300, one 100K-token sequence, 32 / 4 heads (us; 2048-token partitions
+// vs one wave): 4 new tokens 48.0 vs 41.8, 8 tokens 51.5 vs 44.0, 16 tokens
+// 62.0 vs 49.8, 32 tokens (two row tiles) 109.9 vs 76.3; one CTA per SM
+// with rings of 4 + 4 to 6 + 6 stages instead: 47.0, 49.6, 56.3, 97.0.
+//
+// Otherwise, 32 to 128 query rows per KV head (one 128-row tile):
 // V2 at a coarse partition of kTcV2Partition tokens (never finer than the
 // caller's partition_size, and halved down to it while the grid would give
 // fewer CTAs than SMs), or V1 when that partition covers max_seq_len.  The
@@ -650,10 +659,26 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
         *part_out = pc;
         return 2;
     }
-    // CTAs per partition index (one query tile per CTA: the bf16 choice; fp16
-    // may pair tiles, which happens only for many-row steps).
+    // CTAs per partition index, and how many CTAs are resident at once (two
+    // per SM for the one-tile kernel up to head_dim 128, one otherwise).
+    const int tiles = tc_tiles(cols, head_dim, PA_BF16, max_seq_len);
     const long long per_part =
         (long long)num_seqs * num_kv_heads * row_ctas(cols, head_dim, PA_BF16, max_seq_len);
+    const long long slots = (long long)sms * (tiles == 1 && head_dim <= 128 ? 2 : 1);
+    if (2 * per_part <= slots) {
+        // Few (sequence, KV head, row tile) groups: partitions sized so that
+        // the longest sequence's CTAs fill exactly one wave (a multiple of
+        // the 64-token tile), each group split over several SMs.
+        const long long parts = slots / per_part;
+        long long pc = ((long long)max_seq_len + parts - 1) / parts;
+        pc = (pc + kTcTok - 1) / kTcTok * kTcTok;
+        if (pc < partition_size)
+            pc = partition_size;
+        if (pa_v2_num_partitions(max_seq_len, (int)pc) <= 1)
+            return 1;
+        *part_out = (int)pc;
+        return 2;
+    }
     if (cols <= kTcV2MaxRows) {
         int pc = partition_size > kTcV2Partition ? partition_size : kTcV2Partition;
         while (pc / 2 >= partition_size &&

@@ -79,8 +79,12 @@ def test_mq_dispatch_rule_and_entry(cuda_lib):
     assert pa.pa_decode_mq_choose(32, 16, 32, 8, 128, 2048, 512) == 1   # one 2048 partition
     assert pa.pa_decode_mq_partition(32, 16, 32, 8, 128, 2048, 512) == 0
     assert pa.pa_decode_mq_choose(32, 64, 32, 8, 128, 8192, 512) == 1  # 256 rows: V1
-    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 100000, 512) == 2  # one long sequence
-    assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 100000, 512) == 2048
+    assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 100000, 512) == 2  # one long sequence:
+    sms = torch.cuda.get_device_properties(0).multi_processor_count   # one wave of 2 CTAs per SM
+    parts = 2 * sms // 4
+    assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 100000, 512) == -(-(-(-100000 // parts)) // 64) * 64
+    parts = 2 * sms // 8                                                  # 256 rows: two row tiles
+    assert pa.pa_decode_mq_partition(1, 32, 32, 4, 128, 100000, 512) == -(-(-(-100000 // parts)) // 64) * 64
     assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 20000, 512) == 512  # 160 CTAs at 512
     assert pa.pa_decode_mq_choose(1, 16, 32, 4, 128, 512, 512) == 1     # one partition
     for (q_len, G, lens, P) in ((4, 4, (3, 100, 700, 1500), 256),
