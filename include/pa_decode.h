@@ -261,7 +261,10 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
  *     larger, or the grid would leave SMs idle), or V1 when that partition
  *     covers max_seq_len;
  *   - otherwise R > 128 (chunked prefill): V1 when the V1 grid (num_seqs *
- *     num_kv_heads CTAs per 128-row tile) gives every SM a CTA, else V2.
+ *     num_kv_heads CTAs per 128-row tile) gives every SM a CTA -- or, for
+ *     sequences of 8192 tokens and more, V2 on two partitions when V1's
+ *     waves of CTAs would leave more than a tenth of the resident slots
+ *     idle and two partitions pack them better -- else V2.
  * There is no counterpart in the method's description, which dispatches
  * single-token decode only; the rule is measured on GB300.
  */

@@ -626,7 +626,11 @@ int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partitio
 // More rows (chunked prefill): V1 when the V1 grid (num_seqs * num_kv_heads
 // CTAs per row split) gives every SM a CTA, else V2 at the caller's
 // partition size; its partials grow with the rows (chunked prefill, 2 x
-// 2048 new tokens after 30K: V1 2384 vs V2 4867 us at 512 tokens).
+// 2048 new tokens after 30K: V1 2384 vs V2 4867 us at 512 tokens).  When
+// V1's long CTAs would end on a mostly empty wave, V2 on two partitions:
+// the same step, 1024 CTAs in waves of 304, bf16 V1 2456-2526 vs two
+// partitions 2299-2327 us (three: 2357-2375; four: 2355-2388), fp16 1908 vs
+// 1849-1852; 4 x 1024 new tokens after 3072 (short CTAs) V1 332 vs 452.
 // Fewer rows (the mma.sync kernel, 2 or more new tokens): V2 on partitions
 // of max(partition_size, 1024) tokens, halved the same way (us; V1 / V2 at
 // 512 / 1024 / 2048): batch decode, 2 new tokens (8 rows) 96.5 / 86.1 /
@@ -689,7 +693,26 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
         *part_out = pc;
         return 2;
     }
-    return per_part >= sms ? 1 : 2;
+    if (per_part < sms)
+        return 2;
+    // Many rows (chunked prefill), V1's grid fills the SMs: its CTAs run in
+    // waves of `slots`.  When they are long (sequences of 8192 tokens and
+    // more, so that a partial's fixed cost is small beside a CTA's work), the
+    // waves would leave more than a tenth of the slots idle, and two
+    // partitions per sequence pack them better: V2 on two partitions (a
+    // multiple of 64 tokens).  Otherwise V1.
+    const long long waves1 = (per_part + slots - 1) / slots;
+    const long long waves2 = (2 * per_part + slots - 1) / slots;
+    if (max_seq_len >= 4 * kTcV2Partition && 10 * per_part < 9 * slots * waves1 &&
+        waves2 < 2 * waves1 && max_seq_len >= 2 * partition_size) {
+        long long pc = ((long long)max_seq_len + 1) / 2;
+        pc = (pc + kTcTok - 1) / kTcTok * kTcTok;
+        if (pc >= partition_size && pa_v2_num_partitions(max_seq_len, (int)pc) == 2) {
+            *part_out = (int)pc;
+            return 2;
+        }
+    }
+    return 1;
 }
 
 } // namespace

@@ -83,6 +83,14 @@ def test_mq_dispatch_rule_and_entry(cuda_lib):
     sms = torch.cuda.get_device_properties(0).multi_processor_count   # one wave of 2 CTAs per SM
     parts = 2 * sms // 4
     assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 100000, 512) == -(-(-(-100000 // parts)) // 64) * 64
+    # chunked prefill (2 x 2048 new tokens after 30K, 32 / 8 heads): 1024 V1 CTAs in waves of
+    # 2 per SM; two partitions when they pack the waves better
+    n, slots = 2 * 8 * 64, 2 * sms
+    w1, w2 = -(-n // slots), -(-2 * n // slots)
+    two = 10 * n < 9 * slots * w1 and w2 < 2 * w1
+    assert pa.pa_decode_mq_choose(2, 2048, 32, 8, 128, 32768, 512) == (2 if two else 1)
+    assert pa.pa_decode_mq_partition(2, 2048, 32, 8, 128, 32768, 512) == (16384 if two else 0)
+    assert pa.pa_decode_mq_choose(4, 1024, 32, 8, 128, 4096, 512) == 1     # short CTAs: V1
     parts = 2 * sms // 8                                                  # 256 rows: two row tiles
     assert pa.pa_decode_mq_partition(1, 32, 32, 4, 128, 100000, 512) == -(-(-(-100000 // parts)) // 64) * 64
     assert pa.pa_decode_mq_partition(1, 16, 32, 4, 128, 20000, 512) == 512  # 160 CTAs at 512
