@@ -367,6 +367,18 @@ PA_API int pa_set_launch_config(int warps_per_cta, int stages_per_warp);
 PA_API int pa_set_rows_kernel(int mode);
 
 /*
+ * Form of phase 2 (the merge), process-wide: 0 (default) by rule -- one warp
+ * per (row, head) when the longest sequence has at most 8 partitions and
+ * there are more than 16 (row, head) pairs per SM, else one CTA per (head,
+ * row, slice of head_dim); 1 always the CTA-per-slice form; 2 always the
+ * warp-per-pair form (up to 2^30 pairs, else the CTA form).  Both fold the
+ * partitions with the same rule; the choice changes only speed.  Returns
+ * PA_ERR_INVALID_ARG for other values.  A tuning and test hook, with no
+ * counterpart in the method's description.
+ */
+PA_API int pa_set_merge_form(int form);
+
+/*
  * Size of the intermediates array that pa_decode_v2_static keeps inside the
  * library: 16 MiB of device memory on every GPU that loads the library,
  * held until the process exits.

@@ -12,4 +12,5 @@ from ._lib import (  # noqa: F401
     pa_decode_v1, pa_decode_v1_mq, pa_decode_v2, pa_decode_v2_fused, pa_decode_v2_mq,
     pa_decode_v2_phase1,
     pa_decode_v2_phase2, pa_decode_v2_static,
-    pa_selftest_wait_timeout, pa_set_launch_config, pa_set_rows_kernel, status_string, workspace_bytes)
+    pa_selftest_wait_timeout, pa_set_launch_config, pa_set_merge_form, pa_set_rows_kernel, status_string,
+    workspace_bytes)

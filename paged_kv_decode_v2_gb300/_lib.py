@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
     lib.pa_set_launch_config.restype = I
     lib.pa_set_rows_kernel.argtypes = [I]
     lib.pa_set_rows_kernel.restype = I
+    lib.pa_set_merge_form.argtypes = [I]
+    lib.pa_set_merge_form.restype = I
     lib.pa_selftest_wait_timeout.argtypes = [P, ctypes.c_longlong, P]
     lib.pa_selftest_wait_timeout.restype = I
     _lib = lib
@@ -307,6 +309,12 @@ def pa_set_rows_kernel(mode: int = 0) -> None:
     up to 8 rows per KV head, else as 0; 6: tcgen05, one query tile per CTA with the whole
     128-row Q tile stored (modes 0 and 3 store 64 rows for KV heads of at most 64 rows)."""
     _check("pa_set_rows_kernel", load().pa_set_rows_kernel(mode))
+
+
+def pa_set_merge_form(form: int = 0) -> None:
+    """Phase 2's form: 0 by rule; 1 a CTA per (head, row, slice of head_dim); 2 a warp per
+    (row, head)."""
+    _check("pa_set_merge_form", load().pa_set_merge_form(form))
 
 
 def pa_selftest_wait_timeout(status, limit_ns: int, stream=None) -> None:

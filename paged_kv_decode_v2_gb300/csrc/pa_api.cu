@@ -24,6 +24,9 @@ std::atomic<int> g_tune_stages{0};
 // 5 = the CUDA-core (SIMT) kernel up to 8 rows, else as 0, 6 = the one-tile
 // tcgen05 kernel with the whole 128-row Q tile stored at every row count.
 std::atomic<int> g_rows_kernel{0};
+// Phase-2 form: 0 = by rule, 1 = a CTA per (head, row, slice of head_dim),
+// 2 = a warp per (row, head).
+std::atomic<int> g_merge_form{0};
 // From this many query rows per KV head (q_len * G) up, the tcgen05 kernel
 // (128 rows per CTA) runs instead of the mma.sync one (up to 16 per CTA).
 // Measured on GB300 (best of V1 / V2 per kernel, mma.sync vs tcgen05):
@@ -573,7 +576,10 @@ int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_hea
     const int sms = sm_count(dev);
     if (sms <= 0)
         return PA_ERR_CUDA;
-    return launch_merge(dtype, p, num_seqs, sms, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    return launch_merge(dtype, p, num_seqs, sms, g_merge_form.load(std::memory_order_relaxed),
+                        stream) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 int choose_variant(int num_seqs, int num_kv_heads, int max_seq_len, int partition_size, int sms)
@@ -999,6 +1005,14 @@ PA_API int pa_set_rows_kernel(int mode)
     if (mode < 0 || mode > 6)
         return PA_ERR_INVALID_ARG;
     g_rows_kernel.store(mode, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+PA_API int pa_set_merge_form(int form)
+{
+    if (form < 0 || form > 2)
+        return PA_ERR_INVALID_ARG;
+    g_merge_form.store(form, std::memory_order_relaxed);
     return PA_OK;
 }
 

@@ -181,7 +181,10 @@ inline const TcOps *tc_ops(int dtype, int head_dim)
                                                                 : tc_ops_f16_d256();
 }
 
-cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
+// Merge form: 1 one CTA per (head, row, slice of head_dim), 2 one warp per
+// (row, head); `forced` 1 or 2 picks it, 0 lets the rule choose.
+int merge_form(const MergeParams &p, int num_seqs, int num_sms, int forced);
+cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms, int form,
                          cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(int32_t *status, unsigned long long limit_ns, cudaStream_t stream);

@@ -6,12 +6,16 @@
 //     out        = sum_p (rescale_p / sum_q rescale_q) * tmp_output[p]
 // and the self-test kernel of the bounded wait.
 //
-// One CTA per (query head, sequence, slice of head_dim); the slice is at
-// most 128 dims, and smaller (down to 16) when there are few (seq, head)
-// pairs.  A group of lanes owns one partition at a time and reads the
-// slice as float4s (contiguous bytes); the groups of a CTA take partitions
-// round robin, and their running states meet by warp shuffles and then in
-// shared memory.
+// Two forms.  The slice form: one CTA per (query head, sequence, slice of
+// head_dim); the slice is at most 128 dims, and smaller (down to 16) when
+// there are few (seq, head) pairs.  A group of lanes owns one partition at a
+// time and reads the slice as float4s (contiguous bytes); the groups of a
+// CTA take partitions round robin, and their running states meet by warp
+// shuffles and then in shared memory.  The row form: one warp per (row,
+// head), its lanes spanning head_dim, walking the partitions in order --
+// for calls with few partitions and many (row, head) pairs, where a CTA per
+// pair would leave most of its threads idle and the grid's size, not the
+// bytes, would set the time.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -134,6 +138,92 @@ __global__ void __launch_bounds__(NTH) merge_kernel(const MergeParams p)
     }
 }
 
+// The row form: warp w of CTA x merges pair x * kRowWarps + w, i.e. (row,
+// head) with row = pair / num_heads; lane l owns dims [l * DL, l * DL + DL).
+// The partitions are folded in index order with the same running-maximum
+// rule as the slice form.
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_rows_kernel(const MergeParams p, int pairs)
+{
+    using E = Elem<T>;
+    constexpr int DL = D / 32;            // 2, 4 or 8 floats per lane
+    constexpr int kRowWarps = kMergeThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int pair = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (pair >= pairs)
+        return;
+    const int row = pair / p.num_heads;   // (sequence, new token) = b * q_len + i
+    const int b = row / p.q_len;
+    int L = __ldg(&p.seq_lens[b]);
+    L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
+    const int np = (L + p.partition_size - 1) / p.partition_size;
+    T *out = static_cast<T *>(p.out) + (size_t)pair * D + lane * DL;
+    if (np == 0) {
+#pragma unroll
+        for (int j = 0; j < DL; ++j)
+            out[j] = E::from_float(0.f);
+        return;
+    }
+    const float *ml = p.max_logits + (size_t)pair * p.max_num_partitions;
+    const float *es = p.exp_sums + (size_t)pair * p.max_num_partitions;
+    const float *tmp = p.tmp_output + (size_t)pair * p.max_num_partitions * D + lane * DL;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    float m = -INFINITY, l = 0.f;
+    float acc[DL];
+#pragma unroll
+    for (int j = 0; j < DL; ++j)
+        acc[j] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const float mp = __ldg(ml + i);
+        const float lp = __ldg(es + i);
+        float v[DL];
+        if constexpr (DL == 2) {
+            const float2 t = __ldg(reinterpret_cast<const float2 *>(tmp + (size_t)i * D));
+            v[0] = t.x;
+            v[1] = t.y;
+        } else {
+#pragma unroll
+            for (int q = 0; q < DL / 4; ++q) {
+                const float4 t = __ldg(reinterpret_cast<const float4 *>(tmp + (size_t)i * D) + q);
+                v[4 * q] = t.x;
+                v[4 * q + 1] = t.y;
+                v[4 * q + 2] = t.z;
+                v[4 * q + 3] = t.w;
+            }
+        }
+        if (lp == 0.f) // a partition none of whose tokens this query sees
+            continue;
+        const float mn = fmaxf(m, mp);
+        const float a = fast_exp2((m - mn) * kLog2e); // 0 while m is -inf
+        const float w = fast_exp2((mp - mn) * kLog2e) * lp;
+#pragma unroll
+        for (int j = 0; j < DL; ++j)
+            acc[j] = fmaf(acc[j], a, w * v[j]);
+        l = fmaf(l, a, w);
+        m = mn;
+    }
+    const float inv = l > 0.f ? 1.f / l : 0.f; // 0: the query sees no token
+#pragma unroll
+    for (int j = 0; j < DL; ++j)
+        out[j] = E::from_float(acc[j] * inv);
+}
+
+template <typename T>
+static cudaError_t launch_rows_t(cudaLaunchConfig_t &cfg, int head_dim, const MergeParams &p,
+                                 int pairs)
+{
+    switch (head_dim) {
+    case 64: return cudaLaunchKernelEx(&cfg, merge_rows_kernel<T, 64>, p, pairs);
+    case 256: return cudaLaunchKernelEx(&cfg, merge_rows_kernel<T, 256>, p, pairs);
+    default: return cudaLaunchKernelEx(&cfg, merge_rows_kernel<T, 128>, p, pairs);
+    }
+}
+
 template <typename T>
 static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dd, const MergeParams &p)
 {
@@ -145,7 +235,20 @@ static cudaError_t launch_merge_t(cudaLaunchConfig_t &cfg, int dd, const MergePa
     }
 }
 
-cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms,
+int merge_form(const MergeParams &p, int num_seqs, int num_sms, int forced)
+{
+    // The row form's grid counts pairs / 4 CTAs in one dimension: up to 2^30
+    // pairs.
+    const long long pairs = (long long)p.num_heads * num_seqs * p.q_len;
+    if (forced == 1 || (forced == 2 && pairs <= (1LL << 30)))
+        return forced;
+    // Row form when every sequence has at most 8 partitions and the slice
+    // form would launch more than 16 CTAs per SM.
+    const int np_max = (p.seq_len_cap + p.partition_size - 1) / p.partition_size;
+    return np_max <= 8 && pairs > 16LL * num_sms && pairs <= (1LL << 30) ? 2 : 1;
+}
+
+cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms, int form,
                          cudaStream_t stream)
 {
     // A CTA owns at most 128 dims of head_dim (dd); split further, down to 16
@@ -171,8 +274,13 @@ cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_
         else
             break;
     }
+    const long long pairs_all = (long long)p.num_heads * num_seqs * p.q_len;
+    const bool rows = merge_form(p, num_seqs, num_sms, form) == 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.num_heads, num_seqs * p.q_len, p.head_dim / dd);
+    if (rows)
+        cfg.gridDim = dim3((unsigned)((pairs_all + kMergeThreads / 32 - 1) / (kMergeThreads / 32)));
+    else
+        cfg.gridDim = dim3(p.num_heads, num_seqs * p.q_len, p.head_dim / dd);
     cfg.blockDim = dim3(kMergeThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -183,6 +291,11 @@ cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (rows) {
+        if (dtype == PA_BF16)
+            return launch_rows_t<__nv_bfloat16>(cfg, p.head_dim, p, (int)pairs_all);
+        return launch_rows_t<__half>(cfg, p.head_dim, p, (int)pairs_all);
+    }
     if (dtype == PA_BF16)
         return launch_merge_t<__nv_bfloat16>(cfg, dd, p);
     return launch_merge_t<__half>(cfg, dd, p);

@@ -23,7 +23,7 @@ def test_header_declares_the_entry_points():
     for n in ("pa_decode_v2", "pa_decode_v1", "pa_decode", "pa_decode_v2_phase1",
               "pa_decode_v2_phase2", "pa_v2_num_partitions", "pa_v2_workspace_bytes",
               "pa_status_string", "pa_decode_choose", "pa_selftest_wait_timeout",
-              "pa_set_launch_config", "pa_set_rows_kernel", "pa_decode_mq",
+              "pa_set_launch_config", "pa_set_rows_kernel", "pa_set_merge_form", "pa_decode_mq",
               "pa_decode_mq_choose"):
         assert n in names
 
@@ -128,6 +128,14 @@ def test_multi_query_dispatch_validation(cuda_lib):
     assert lib.pa_decode_mq(*args, 512, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
     args = [FAKE] * 5 + [1, 4, 8, 2, 128, 128, 16, 63, 0, 0.088]
     assert lib.pa_decode_mq(*args, 0, 0, FAKE, FAKE, FAKE, FAKE, 2, None, None) == 1
+
+
+def test_merge_form_override_validation(cuda_lib):
+    lib = cuda_lib.load()
+    assert lib.pa_set_merge_form(-1) == 1
+    assert lib.pa_set_merge_form(3) == 1
+    for f in (2, 1, 0):
+        assert lib.pa_set_merge_form(f) == 0
 
 
 def test_rows_kernel_override_validation(cuda_lib):
