@@ -13,13 +13,14 @@ partitions that begin inside a block, K and V rings of one to five stages, chunk
 prefill (a chunk of new tokens attending to a cached prefix and causally to
 itself), poisoned caches and bad block ids.
 """
+import numpy as np
 import pytest
 import torch
 
 import oracle
 import workloads as wl
-from parity_util import (check_mq, check_out, check_partitions, mq, oracle_problem, run_mq,
-                         run_v2)
+from parity_util import (OUT_ABS, check_mq, check_out, check_partitions, half_ulp, mq,
+                         oracle_problem, run_mq, run_v2)
 
 pytestmark = pytest.mark.gpu
 
@@ -104,6 +105,40 @@ def test_tc_chunked_prefill(q_len, prefix, dtype):
     lens = (prefix + q_len, q_len + 5)
     w = mq("tc_prefill", q_len, 4, lens, P=512, dtype=dtype, seed=8500 + q_len + prefix + dtype)
     check_mq(wl.make_inputs(w, device="cuda"), 512)
+
+
+@pytest.mark.parametrize("dtype", [wl.F16, wl.BF16])
+def test_tc_values_beyond_binary16(dtype):
+    """V values of magnitude 2^16 and more in a few visible tokens (first, middle and last K/V
+    tile of a sequence; fp16 storage gets values near its own limit instead), through every
+    tcgen05 kernel form.
+
+    Tolerance: the parity bound (2e-3 plus half an ulp of the output) assumes V of unit scale.
+    P is rounded to the storage type before P.V (11 significant bits for fp16; hi + lo halves,
+    about 16, for bf16), so each term p * v moves by at most 2^-12 of p * |v|; this test adds
+    2^-11 * sum(p |v|) / l, the oracle's output on |V|, to that bound.  A large value lost or
+    clamped anywhere on the way would miss it by far."""
+    P = 512
+    lens = (300, 1100, 2000)
+    w = mq("tc_wide", 40, 4, lens, P=P, dtype=dtype, seed=8750 + dtype)  # 160 rows per KV head
+    inp = wl.make_inputs(w, device="cuda")
+    big = [7.0e4, -2.5e5, 65536.0, -1.0e6] if dtype == wl.BF16 else [6.0e4, -6.5e4, 3.0e4, -5.0e4]
+    bs = w.block_size
+    tables = inp.block_tables.cpu()
+    for b, L in enumerate(lens):
+        for k, t in enumerate((5, L // 2, L - 1)):
+            blk = int(tables[b, t // bs])
+            inp.value_cache[blk, :, t % bs, (7 * k + b) % w.head_dim] = big[(k + b) % len(big)]
+    arrays = wl.to_oracle_arrays(inp)
+    ref = oracle.decode(oracle.Problem.from_arrays(arrays))
+    arrays["value_cache"] = arrays["value_cache"] & np.uint16(0x7FFF)  # |V|: sign bit cleared
+    ref_abs = oracle.decode(oracle.Problem.from_arrays(arrays))
+    tol = OUT_ABS + half_ulp(ref, dtype) + 2.0 ** -11 * ref_abs
+    for e in ("v2", "v1"):
+        out = run_mq(inp, P, entry=e)[0].cpu().to(torch.float64).numpy()
+        assert np.isfinite(out).all(), e
+        err = np.abs(out - ref)
+        assert (err <= tol).all(), (e, int((err > tol).sum()), float((err - tol).max()))
 
 
 def ramp_scores(inp, c, period=None):
