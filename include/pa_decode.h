@@ -286,7 +286,28 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * its max_seq_len), V2 at the partition size pa_decode_mq_partition returns.
  * The V2 intermediates, sized for partition_size, must be valid whenever V2
  * can be chosen; after a V2 call they hold the partials of that (possibly
- * coarser) partitioning.
+ * coarser) partitioning -- at a stride of max_num_partitions, except in the
+ * case below.
+ *
+ * bf16 caches whose rows take the two-tile tcgen05 kernel (R > 128,
+ * head_dim <= 128, max_seq_len >= 1024; pa_set_rows_kernel 0, 2 or 4):
+ * tmp_output, when given and large enough, also holds a binary16 copy of
+ * the V blocks the call reads, and P.V runs on binary16 P and V (one MMA per
+ * K-step where bf16 needs a hi + lo pair of P halves).  Layout, in bytes from
+ * tmp_output: the partials at a stride of the partitions used (np, 0 for
+ * V1), num_seqs * q_len * num_heads * np * head_dim * 4 bytes; at the next
+ * multiple of 256 the copy, [num_seqs][num_kv_heads][max_blocks_per_seq]
+ * [block_size][head_dim] binary16 (a sequence's logical block j at index
+ * j, rows past its end zero, an out-of-range block id read as block 0); at
+ * the next multiple of 256 after it a 32-bit flag, set to 1 when a finite
+ * value of magnitude 2^16 or more was met (binary16 cannot hold it): the
+ * call then reads the bf16 cache with P in hi + lo halves instead.  Every
+ * bf16 value below 2^16 has an exact binary16 form, so the copy loses
+ * nothing.  When tmp_output (num_seqs * q_len * num_heads *
+ * max_num_partitions * head_dim * 4 bytes) cannot hold all three, or the
+ * copy's rows exceed 2^31, there is no copy and the call runs the one-tile
+ * kernel with hi + lo P.  The copy adds one read and one write of the V
+ * blocks' bytes to the call.
  */
 PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
                         const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,

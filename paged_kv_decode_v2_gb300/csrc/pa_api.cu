@@ -16,6 +16,13 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// A binary16 copy of the V blocks of one multi-query call (bf16 caches) and
+// the flag word that says whether it holds every value exactly.
+struct VhCopy {
+    void *copy;
+    int32_t *flag;
+};
+
 std::atomic<int> g_tune_warps{0};
 std::atomic<int> g_tune_stages{0};
 // Kernel for the query rows of a KV head: 0 = by row count, 1 = always the
@@ -420,7 +427,8 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
                int max_blocks_per_seq, int cap, float scale, int dtype, bool v1,
                int num_partitions, int partition_size,
                float *tmp_output, float *exp_sums, float *max_logits, int max_num_partitions,
-               void *out, int32_t *status, int32_t *counters = nullptr)
+               void *out, int32_t *status, int32_t *counters = nullptr,
+               const VhCopy *vh = nullptr)
 {
     L = AttnLaunch{};
     // The fused V2 (counters given) runs on the mma.sync kernel at any row count.
@@ -433,6 +441,16 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
                           head_dim);
     if (rc)
         return rc;
+    if (vh) {
+        // The copy is [S][KV][max_blocks][block_size][head_dim] binary16: the
+        // cache map's shape with S * max_blocks blocks.
+        rc = encode_cache_map(&L.tmap_vh, vh->copy, PA_F16, num_seqs * max_blocks_per_seq,
+                              num_kv_heads, block_size, head_dim);
+        if (rc)
+            return rc;
+    }
+    // With the binary16 copy, bf16 rows take the kernel fp16's would.
+    const int tile_dtype = vh ? PA_F16 : dtype;
     AttnParams &p = L.p;
     p.query = query;
     p.block_tables = block_tables;
@@ -446,13 +464,13 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     if (L.tc) {
         // 128 rows per query tile; the CTAs of one range split the rows.
         L.cta_cols = kMaxGroup;
-        L.tc_tiles = tc_tiles(p.cols, head_dim, dtype, cap);
+        L.tc_tiles = tc_tiles(p.cols, head_dim, tile_dtype, cap);
         // At most 64 rows on one tile: only Q rows 64-127 are stored.
         p.q_half = (L.tc_tiles == 1 && p.cols <= kTcRows / 2 &&
                     g_rows_kernel.load(std::memory_order_relaxed) != 6)
                        ? 1
                        : 0;
-        p.col_groups = row_ctas(p.cols, head_dim, dtype, cap);
+        p.col_groups = row_ctas(p.cols, head_dim, tile_dtype, cap);
     } else {
         // Up to 8 query rows: one n-tile (or the SIMT kernel when asked for);
         // more: 16 per CTA, split over CTAs.
@@ -471,6 +489,7 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.max_logits = max_logits;
     p.out = out;
     p.counters = counters;
+    p.vh_flag = vh && L.tc && L.tc_tiles == 2 ? vh->flag : nullptr;
     p.status = status;
     L.fused = fused;
     L.head_dim = head_dim;
@@ -498,7 +517,8 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
                    int max_blocks_per_seq, int max_seq_len_hint, float scale, int partition_size,
                    int dtype, float *tmp_output, float *exp_sums, float *max_logits,
                    int max_num_partitions, int32_t *status, cudaStream_t stream, int *cap_out,
-                   void *fused_out = nullptr, int32_t *counters = nullptr)
+                   void *fused_out = nullptr, int32_t *counters = nullptr,
+                   const VhCopy *vh = nullptr)
 {
     int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
                          num_heads, num_kv_heads, head_dim, num_blocks, block_size,
@@ -527,7 +547,7 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
     rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
                     num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
                     cap, scale, dtype, false, np, partition_size, tmp_output, exp_sums, max_logits,
-                    max_num_partitions, fused_out, status, counters);
+                    max_num_partitions, fused_out, status, counters, vh);
     if (rc)
         return rc;
     return prepare_and_launch_attn(L, stream);
@@ -721,6 +741,59 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
     return 1;
 }
 
+
+// V2 for several new tokens (phase 1 and the merge); vh: a binary16 copy of
+// V for the two-tile kernel, or null.
+int v2_mq_impl(const void *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int q_len,
+               int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+               int max_blocks_per_seq, int max_seq_len_hint, float scale, int partition_size,
+               int dtype, void *out, float *tmp_output, float *exp_sums, float *max_logits,
+               int max_num_partitions, int32_t *status, cudaStream_t stream, const VhCopy *vh)
+{
+    if (!out || !aligned(out, 4))
+        return PA_ERR_INVALID_ARG;
+    int cap = 0;
+    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
+                            tmp_output, exp_sums, max_logits, max_num_partitions, status, stream,
+                            &cap, nullptr, nullptr, vh);
+    if (rc)
+        return rc;
+    return v2_phase2_impl(seq_lens, num_seqs, q_len, num_heads, head_dim, cap, partition_size,
+                          dtype, tmp_output, exp_sums, max_logits, max_num_partitions, out, status,
+                          stream);
+}
+
+// V1 for several new tokens; vh as for v2_mq_impl.
+int v1_mq_impl(const void *query, const void *key_cache, const void *value_cache,
+               const int32_t *block_tables, const int32_t *seq_lens, int num_seqs, int q_len,
+               int num_heads, int num_kv_heads, int head_dim, int num_blocks, int block_size,
+               int max_blocks_per_seq, int max_seq_len_hint, float scale, int dtype, void *out,
+               int32_t *status, cudaStream_t stream, const VhCopy *vh)
+{
+    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                         max_blocks_per_seq, scale, dtype);
+    if (rc)
+        return rc;
+    rc = check_q_len(num_seqs, q_len);
+    if (rc)
+        return rc;
+    if (!out || !aligned(out, 4) || (status && !aligned(status, 4)))
+        return PA_ERR_INVALID_ARG;
+    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
+    AttnLaunch L;
+    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                    cap, scale, dtype, true, 1, 0, nullptr, nullptr, nullptr, 0, out, status,
+                    nullptr, vh);
+    if (rc)
+        return rc;
+    return prepare_and_launch_attn(L, stream);
+}
+
 } // namespace
 
 extern "C" {
@@ -774,19 +847,10 @@ PA_API int pa_decode_v2_mq(const void *query, const void *key_cache, const void 
                            void *out, float *tmp_output, float *exp_sums, float *max_logits,
                            int max_num_partitions, int32_t *status, pa_stream_t stream)
 {
-    if (!out || !aligned(out, 4))
-        return PA_ERR_INVALID_ARG;
-    int cap = 0;
-    int rc = v2_phase1_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
-                            num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                            max_blocks_per_seq, max_seq_len_hint, scale, partition_size, dtype,
-                            tmp_output, exp_sums, max_logits, max_num_partitions, status,
-                            (cudaStream_t)stream, &cap);
-    if (rc)
-        return rc;
-    return v2_phase2_impl(seq_lens, num_seqs, q_len, num_heads, head_dim, cap, partition_size,
-                          dtype, tmp_output, exp_sums, max_logits, max_num_partitions, out, status,
-                          (cudaStream_t)stream);
+    return v2_mq_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                      num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                      max_seq_len_hint, scale, partition_size, dtype, out, tmp_output, exp_sums,
+                      max_logits, max_num_partitions, status, (cudaStream_t)stream, nullptr);
 }
 
 PA_API int pa_decode_v2(const void *query, const void *key_cache, const void *value_cache,
@@ -830,24 +894,9 @@ PA_API int pa_decode_v1_mq(const void *query, const void *key_cache, const void 
                            int max_seq_len_hint, float scale, int dtype, void *out,
                            int32_t *status, pa_stream_t stream)
 {
-    int rc = check_shape(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
-                         num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                         max_blocks_per_seq, scale, dtype);
-    if (rc)
-        return rc;
-    rc = check_q_len(num_seqs, q_len);
-    if (rc)
-        return rc;
-    if (!out || !aligned(out, 4) || (status && !aligned(status, 4)))
-        return PA_ERR_INVALID_ARG;
-    const int cap = seq_cap(max_blocks_per_seq, block_size, max_seq_len_hint);
-    AttnLaunch L;
-    rc = build_attn(L, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
-                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
-                    cap, scale, dtype, true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
-    if (rc)
-        return rc;
-    return prepare_and_launch_attn(L, (cudaStream_t)stream);
+    return v1_mq_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                      num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                      max_seq_len_hint, scale, dtype, out, status, (cudaStream_t)stream, nullptr);
 }
 
 PA_API int pa_decode_v1(const void *query, const void *key_cache, const void *value_cache,
@@ -937,15 +986,64 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
                                 : partition_size;
     if (part < 0)
         return -part;
+    const cudaStream_t st = (cudaStream_t)stream;
+    // The arguments the entry points below check, checked here too: nothing
+    // may be launched for a call that is then refused.
+    if (!out || !aligned(out, 4) || (status && !aligned(status, 4)))
+        return PA_ERR_INVALID_ARG;
+    if (which == 2 && (!tmp_output || !exp_sums || !max_logits || max_num_partitions <= 0 ||
+                       !aligned(tmp_output, 16) || !aligned(exp_sums, 4) ||
+                       !aligned(max_logits, 4)))
+        return PA_ERR_INVALID_ARG;
+    if (which == 2 && pa_v2_num_partitions(cap, part) > max_num_partitions)
+        return PA_ERR_WORKSPACE;
+    // bf16 rows that would take the two-tile kernel as fp16's do: a binary16
+    // copy of the V blocks, in tmp_output past the partials (written at a
+    // stride of the partitions actually used), when it fits.
+    VhCopy vh{nullptr, nullptr};
+    int np_used = 0;
+    const int cols = q_len * (num_heads / num_kv_heads);
+    if (dtype == PA_BF16 && use_tc(cols) && tc_tiles(cols, head_dim, PA_F16, cap) == 2 &&
+        tmp_output && aligned(tmp_output, 16) && max_num_partitions > 0) {
+        np_used = which == 2 ? pa_v2_num_partitions(cap, part) : 0;
+        const size_t used = (size_t)num_seqs * q_len * num_heads * np_used * head_dim * 4;
+        const size_t off = (used + 255) & ~(size_t)255;
+        const size_t copy_bytes =
+            (size_t)num_seqs * num_kv_heads * max_blocks_per_seq * block_size * head_dim * 2;
+        const size_t have =
+            (size_t)num_seqs * q_len * num_heads * (size_t)max_num_partitions * head_dim * 4;
+        const long long rows = (long long)num_seqs * max_blocks_per_seq * num_kv_heads * block_size;
+        const size_t need = off + ((copy_bytes + 255) & ~(size_t)255) + 256;
+        if (rows <= INT32_MAX && np_used <= max_num_partitions && need <= have) {
+            char *base = reinterpret_cast<char *>(tmp_output) + off;
+            vh.copy = base;
+            vh.flag = reinterpret_cast<int32_t *>(base + ((copy_bytes + 255) & ~(size_t)255));
+            VhParams vp;
+            vp.value_cache = value_cache;
+            vp.block_tables = block_tables;
+            vp.seq_lens = seq_lens;
+            vp.num_kv_heads = num_kv_heads;
+            vp.head_dim = head_dim;
+            vp.block_size = block_size;
+            vp.num_blocks = num_blocks;
+            vp.max_blocks = max_blocks_per_seq;
+            vp.seq_len_cap = cap;
+            vp.copy = vh.copy;
+            vp.flag = vh.flag;
+            if (cudaMemsetAsync(vh.flag, 0, sizeof(int32_t), st) != cudaSuccess ||
+                launch_v_half(vp, num_seqs, st) != cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+    }
+    const VhCopy *vhp = vh.copy ? &vh : nullptr;
     if (which == 1)
-        return pa_decode_v1_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
-                               q_len, num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                               max_blocks_per_seq, max_seq_len_hint, scale, dtype, out, status,
-                               stream);
-    return pa_decode_v2_mq(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
-                           num_heads, num_kv_heads, head_dim, num_blocks, block_size,
-                           max_blocks_per_seq, max_seq_len_hint, scale, part, dtype, out,
-                           tmp_output, exp_sums, max_logits, max_num_partitions, status, stream);
+        return v1_mq_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                          num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                          max_blocks_per_seq, max_seq_len_hint, scale, dtype, out, status, st, vhp);
+    return v2_mq_impl(query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                      num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                      max_seq_len_hint, scale, part, dtype, out, tmp_output, exp_sums, max_logits,
+                      vhp ? np_used : max_num_partitions, status, st, vhp);
 }
 
 PA_API int pa_decode(const void *query, const void *key_cache, const void *value_cache,

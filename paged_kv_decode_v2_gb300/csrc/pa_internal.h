@@ -48,6 +48,7 @@ struct AttnParams {
     float *max_logits;           // V2: [S, q_len, H, NPcap]
     void *out;                   // V1 and fused V2: [S, q_len, H, D]
     int32_t *counters;           // fused V2: [S, KV] tickets, zero between calls
+    const int32_t *vh_flag;      // two-tile bf16: a binary16 copy of V exists; nonzero = not usable
     int32_t *status;
 };
 
@@ -55,6 +56,7 @@ struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
+    CUtensorMap tmap_vh;         // the binary16 copy of V (two-tile bf16 with vh_flag)
     int head_dim;                // 64, 128 or 256
     int block_size;              // 8, 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
@@ -83,6 +85,24 @@ struct MergeParams {
     void *out;
     int32_t *status;
 };
+
+// The binary16 copy of the V blocks a multi-query call reads (bf16 caches):
+// [S][KV][max_blocks][block_size][head_dim], rows past a sequence's end zero,
+// and a flag word set when a finite value is 2^16 or more in magnitude.
+struct VhParams {
+    const void *value_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    int num_kv_heads;
+    int head_dim;
+    int block_size;
+    int num_blocks;
+    int max_blocks;
+    int seq_len_cap;
+    void *copy;
+    int32_t *flag;
+};
+cudaError_t launch_v_half(const VhParams &p, int num_seqs, cudaStream_t stream);
 
 // Per-warp shared-memory ring bytes for one stage: a K tile and a V tile of
 // block_size rows (at least 16: an 8-token block size stages two blocks) x

@@ -656,8 +656,14 @@ static cudaError_t tc_launch(const AttnLaunch &L, cudaStream_t stream)
     const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1, L.tc_tiles);
     if (!fn)
         return cudaErrorInvalidValue;
-    void *args[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
-                    const_cast<AttnParams *>(&L.p)};
+    // The two-tile kernel also takes the binary16 copy's map (the V map when
+    // there is no copy; it is then not read).
+    const CUtensorMap *vh = L.p.vh_flag ? &L.tmap_vh : &L.tmap_v;
+    void *args1[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
+                     const_cast<AttnParams *>(&L.p)};
+    void *args2[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
+                     const_cast<CUtensorMap *>(vh), const_cast<AttnParams *>(&L.p)};
+    void **args = L.tc_tiles == 2 ? args2 : args1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = L.grid;
     cfg.blockDim = dim3(L.tc_tiles == 2 ? kTc2Threads : kTcThreads);

@@ -23,6 +23,12 @@
 // Warp roles: warps 0-3 own the rows of tile 0 and warps 4-7 those of tile
 // 1 (one row per thread), warp 8 issues the MMAs and owns the TMEM
 // allocation, two lanes of warp 9 load the K and V tiles with TMA.
+//
+// bf16 caches: when the call made a binary16 copy of its V blocks
+// (pa_vhalf.cu) and found no value it cannot hold (*vh_flag == 0), V comes
+// from that copy and P.V runs on binary16 P and V, one MMA per K-step, as
+// for fp16 caches; otherwise P is split into bf16 hi + lo halves.  S = Q K^T
+// stays in bf16.
 #pragma once
 
 #include "pa_device.cuh"
@@ -46,7 +52,8 @@ struct Tc2Cfg {
 template <typename T, int D, int BS, bool V1>
 __global__ void __launch_bounds__(kTc2Threads)
     tc2_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v, const AttnParams p)
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_vh, const AttnParams p)
 {
     static_assert(D <= 128, "two query tiles need O + S of each in 256 TMEM columns");
     using C = Tc2Cfg<D>;
@@ -70,6 +77,9 @@ __global__ void __launch_bounds__(kTc2Threads)
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    // V from the binary16 copy (bf16 caches, copy made and usable): uniform
+    // over the CTA.
+    const bool use_h = kBf16 && p.vh_flag != nullptr && __ldcg(p.vh_flag) == 0;
 
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {
@@ -191,7 +201,10 @@ __global__ void __launch_bounds__(kTc2Threads)
         // once P.V of both is.  Block ids are fetched a tile ahead.
         if (lane < 2) {
             const bool is_k = lane == 0;
-            const CUtensorMap *map = is_k ? &tmap_k : &tmap_v;
+            const CUtensorMap *map = is_k ? &tmap_k : use_h ? &tmap_vh : &tmap_v;
+            // Row of block k of tile t in the binary16 copy: the sequence's
+            // logical block blk0 + t * kBPT + k.
+            const long long vh_row0 = ((long long)b * p.num_kv_heads + kv) * p.max_blocks + blk0;
             const uint32_t ring = is_k ? k_sm : v_sm;
             const uint32_t full = is_k ? b_k_full : b_v_full;
             const uint32_t empty = is_k ? b_k_empty : b_v_empty;
@@ -233,7 +246,9 @@ __global__ void __launch_bounds__(kTc2Threads)
 #pragma unroll
                 for (int k = 0; k < kBPT; ++k) {
                     if (k < nb) {
-                        const int row = (int)(((long long)ids[k] * p.num_kv_heads + kv) * BS);
+                        const int row =
+                            !is_k && use_h ? (int)((vh_row0 + t * kBPT + k) * BS)
+                                           : (int)(((long long)ids[k] * p.num_kv_heads + kv) * BS);
 #pragma unroll
                         for (int sl = 0; sl < C::kSlices; ++sl)
                             tma_load_3d(ring + s * C::kKVBytes + sl * C::kKVSlice + k * BS * 128, map,
@@ -255,6 +270,8 @@ __global__ void __launch_bounds__(kTc2Threads)
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16<kBf16>(kTcRows, kTc2Tok, false);
             constexpr uint32_t idesc_o = idesc_f16<kBf16>(kTcRows, D, true);
+            constexpr uint32_t idesc_o16 = idesc_f16<false>(kTcRows, D, true);
+            const bool split = kBf16 && !use_h; // P in hi + lo halves
             // Descriptors are linear in the address (start / 16 in the low
             // bits, shared memory < 256 KB): offsets are added to a base.
             const uint64_t qd = smem_desc_sw128(q_sm, 16, 1024);
@@ -282,8 +299,9 @@ __global__ void __launch_bounds__(kTc2Threads)
                 for (int kt = 0; kt < kTc2Tok / 16; ++kt) {
                     const uint32_t a = pc + 32 * (kt >> 1) + 8 * (kt & 1);
                     const uint64_t bd = vb + ((kt * 2048) >> 4);
-                    tc_mma_ts(tmem + qq * C::kTileCols, a, bd, idesc_o, (t > 0 || kt > 0) ? 1u : 0u);
-                    if (kBf16)
+                    tc_mma_ts(tmem + qq * C::kTileCols, a, bd, split ? idesc_o : idesc_o16,
+                              (t > 0 || kt > 0) ? 1u : 0u);
+                    if (split)
                         tc_mma_ts(tmem + qq * C::kTileCols, a + 16, bd, idesc_o, 1u);
                 }
             };
@@ -441,21 +459,31 @@ __global__ void __launch_bounds__(kTc2Threads)
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
                     uint32_t ph[16], pl[16];
-#pragma unroll
-                    for (int c = 0; c < 32; c += 2) {
-                        const float x0 = __uint_as_float(sr[k][c]), x1 = __uint_as_float(sr[k][c + 1]);
-                        const float p0 = fast_exp2(fmaf(x0, cf, -mb));
-                        const float p1 = fast_exp2(fmaf(x1, cf, -mb));
-                        ls[(c >> 1) & 3] += p0 + p1;
-                        const uint32_t hh = E::pack(p0, p1);
-                        ph[c >> 1] = hh;
-                        pl[c >> 1] = kBf16 ? E::pack(p0 - E::lo(hh), p1 - E::hi(hh)) : 0u;
-                    }
                     const uint32_t col = s_col + 64 * h + 32 * k;
-                    if (kBf16)
+                    if (kBf16 && !use_h) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float x0 = __uint_as_float(sr[k][c]), x1 = __uint_as_float(sr[k][c + 1]);
+                            const float p0 = fast_exp2(fmaf(x0, cf, -mb));
+                            const float p1 = fast_exp2(fmaf(x1, cf, -mb));
+                            ls[(c >> 1) & 3] += p0 + p1;
+                            const uint32_t hh = E::pack(p0, p1);
+                            ph[c >> 1] = hh;
+                            pl[c >> 1] = E::pack(p0 - E::lo(hh), p1 - E::hi(hh));
+                        }
                         tmem_st16x2(col, ph, col + 16, pl);
-                    else
+                    } else {
+                        // binary16 P: fp16 caches, or bf16 with V from the copy
+#pragma unroll
+                        for (int c = 0; c < 32; c += 2) {
+                            const float x0 = __uint_as_float(sr[k][c]), x1 = __uint_as_float(sr[k][c + 1]);
+                            const float p0 = fast_exp2(fmaf(x0, cf, -mb));
+                            const float p1 = fast_exp2(fmaf(x1, cf, -mb));
+                            ls[(c >> 1) & 3] += p0 + p1;
+                            ph[c >> 1] = Elem<__half>::pack(p0, p1);
+                        }
                         tmem_st16(col, ph);
+                    }
                 }
             }
             l_run = fmaf(l_run, a, (ls[0] + ls[1]) + (ls[2] + ls[3]));
