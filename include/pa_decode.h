@@ -301,7 +301,9 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * j, rows past its end zero, an out-of-range block id read as block 0); at
  * the next multiple of 256 after it a 32-bit flag, set to 1 when a finite
  * value of magnitude 2^16 or more was met (binary16 cannot hold it): the
- * call then reads the bf16 cache with P in hi + lo halves instead.  Every
+ * call then reads the bf16 cache with P in hi + lo halves instead (the
+ * binary16 kernel and a one-tile bf16 kernel are both launched; each reads
+ * the flag first and one of them returns at once).  Every
  * bf16 value below 2^16 has an exact binary16 form, so the copy loses
  * nothing.  When tmp_output (num_seqs * q_len * num_heads *
  * max_num_partitions * head_dim * 4 bytes) cannot hold all three, or the

@@ -299,14 +299,15 @@ void size_attn(AttnLaunch &L, int dev, int sms, size_t limit)
 }
 
 // Per-device dynamic shared memory limit of each tcgen05 kernel after the opt-in.
-constexpr int kTcSlots = 2 * 3 * 4 * 2 * 2;
+constexpr int kTcSlots = 2 * 3 * 4 * 2 * 2 * 2;
 std::atomic<int> g_tc_smem_limit[kMaxDevices][kTcSlots];
 
-int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles)
+int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles, bool vh)
 {
     const int di = head_dim == 64 ? 0 : head_dim == 128 ? 1 : 2;
     const int bi = block_size == 8 ? 3 : block_size == 16 ? 0 : block_size == 32 ? 1 : 2;
-    return ((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 2 + (v1 ? 1 : 0)) * 2 + (tiles - 1);
+    return (((((dtype == PA_BF16 ? 1 : 0) * 3 + di) * 4 + bi) * 2 + (v1 ? 1 : 0)) * 2 +
+            (tiles - 1)) * 2 + (vh ? 1 : 0);
 }
 
 // The tcgen05 kernels.  One query tile: as many K and V ring stages as keep
@@ -321,13 +322,13 @@ int tc_slot(int dtype, int head_dim, int block_size, bool v1, int tiles)
 int prepare_and_launch_tc(AttnLaunch &L, int dev, cudaStream_t stream)
 {
     const int tiles = L.tc_tiles;
-    const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1, tiles);
+    const int slot = tc_slot(L.dtype, L.head_dim, L.block_size, L.v1, tiles, L.vh);
     size_t limit = (size_t)g_tc_smem_limit[dev][slot].load(std::memory_order_acquire);
     if (limit == 0) {
         int optin = 0;
         if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
             return PA_ERR_CUDA;
-        if (tc_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.v1, tiles, optin, &limit) !=
+        if (tc_ops(L.dtype, L.head_dim)->prepare(L.block_size, L.v1, tiles, L.vh, optin, &limit) !=
             cudaSuccess)
             return PA_ERR_CUDA;
         g_tc_smem_limit[dev][slot].store((int)limit, std::memory_order_release);
@@ -395,7 +396,8 @@ bool use_tc(int cols)
 // need head_dim <= 128.  By default they are taken for fp16 when a KV head
 // has more than 128 rows and sequences reach 1024 tokens; bf16, whose split
 // P doubles the P.V work, and short sequences run faster with one tile and
-// two CTAs per SM.  Measured on GB300 (V1, one vs two tiles): chunked prefill
+// two CTAs per SM.  (The multi-query dispatch gives bf16 the fp16 rule when it
+// can make a binary16 copy of V: pa_decode_mq.)  Measured on GB300 (V1, one vs two tiles): chunked prefill
 // (2 x 2048 new tokens after 30K) bf16 2384 vs 2495 us, fp16 2137 vs 1903;
 // 4 x 1024 new after 3072 bf16 323 vs 351, fp16 296 vs 282; 8 x 512 new
 // tokens, no prefix, fp16 75 vs 87.
@@ -489,9 +491,9 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     p.max_logits = max_logits;
     p.out = out;
     p.counters = counters;
-    p.vh_flag = vh && L.tc && L.tc_tiles == 2 ? vh->flag : nullptr;
     p.status = status;
     L.fused = fused;
+    L.vh = vh && L.tc && L.tc_tiles == 2 && dtype == PA_BF16;
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.dtype = dtype;
@@ -550,7 +552,25 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
                     max_num_partitions, fused_out, status, counters, vh);
     if (rc)
         return rc;
-    return prepare_and_launch_attn(L, stream);
+    if (!L.vh)
+        return prepare_and_launch_attn(L, stream);
+    // The binary16 form, then the bf16 form behind it: each does the work or
+    // nothing, by the copy's flag (set: a value the copy cannot hold).
+    L.p.skip_if = vh->flag;
+    L.p.skip_val = 1;
+    rc = prepare_and_launch_attn(L, stream);
+    if (rc)
+        return rc;
+    AttnLaunch F;
+    rc = build_attn(F, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                    cap, scale, dtype, false, np, partition_size, tmp_output, exp_sums, max_logits,
+                    max_num_partitions, fused_out, status, counters, nullptr);
+    if (rc)
+        return rc;
+    F.p.skip_if = vh->flag;
+    F.p.skip_val = 0;
+    return prepare_and_launch_attn(F, stream);
 }
 
 int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_heads, int head_dim,
@@ -791,7 +811,23 @@ int v1_mq_impl(const void *query, const void *key_cache, const void *value_cache
                     nullptr, vh);
     if (rc)
         return rc;
-    return prepare_and_launch_attn(L, stream);
+    if (!L.vh)
+        return prepare_and_launch_attn(L, stream);
+    // As in v2_phase1_impl: the binary16 form, then the bf16 form behind it.
+    L.p.skip_if = vh->flag;
+    L.p.skip_val = 1;
+    rc = prepare_and_launch_attn(L, stream);
+    if (rc)
+        return rc;
+    AttnLaunch F;
+    rc = build_attn(F, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
+                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                    cap, scale, dtype, true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
+    if (rc)
+        return rc;
+    F.p.skip_if = vh->flag;
+    F.p.skip_val = 0;
+    return prepare_and_launch_attn(F, stream);
 }
 
 } // namespace

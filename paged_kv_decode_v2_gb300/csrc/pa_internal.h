@@ -48,7 +48,8 @@ struct AttnParams {
     float *max_logits;           // V2: [S, q_len, H, NPcap]
     void *out;                   // V1 and fused V2: [S, q_len, H, D]
     int32_t *counters;           // fused V2: [S, KV] tickets, zero between calls
-    const int32_t *vh_flag;      // two-tile bf16: a binary16 copy of V exists; nonzero = not usable
+    const int32_t *skip_if;      // when non-null: the grid does nothing if *skip_if == skip_val
+    int skip_val;
     int32_t *status;
 };
 
@@ -56,7 +57,7 @@ struct AttnLaunch {
     AttnParams p;
     CUtensorMap tmap_k;
     CUtensorMap tmap_v;
-    CUtensorMap tmap_vh;         // the binary16 copy of V (two-tile bf16 with vh_flag)
+    CUtensorMap tmap_vh;         // the binary16 copy of V (two-tile bf16 kernel reading it)
     int head_dim;                // 64, 128 or 256
     int block_size;              // 8, 16, 32 or 64
     int dtype;                   // PA_F16 / PA_BF16
@@ -65,6 +66,7 @@ struct AttnLaunch {
     bool simt;                   // the CUDA-core kernel (up to 8 rows) instead of mma.sync
     bool tc;                     // a tcgen05 kernel
     int tc_tiles;                // its 128-row query tiles per CTA (1 or 2)
+    bool vh;                     // two tiles, bf16: V from the binary16 copy, binary16 P.V
     int cta_cols;                // query rows one CTA serves (<= 16): picks the n-tile count
     dim3 grid;
     int warps;
@@ -182,7 +184,8 @@ inline size_t tc2_smem_bytes(int head_dim, int k_stages, int v_stages)
 
 // Entry points of the tcgen05 attention kernels for one (storage type, head_dim).
 struct TcOps {
-    cudaError_t (*prepare)(int block_size, bool v1, int tiles, int optin_bytes, size_t *limit);
+    cudaError_t (*prepare)(int block_size, bool v1, int tiles, bool vh, int optin_bytes,
+                           size_t *limit);
     cudaError_t (*launch)(const AttnLaunch &L, cudaStream_t stream);
 };
 const TcOps *tc_ops_f16_d64();

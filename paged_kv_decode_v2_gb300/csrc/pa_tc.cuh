@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     // the previous grid in the stream has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
+    // A fallback launch whose work another grid has done (AttnParams::skip_if).
+    if (p.skip_if && __ldcg(p.skip_if) == p.skip_val)
+        return;
 
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {
@@ -609,16 +612,31 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     }
 }
 
-// Kernel dispatch on block size, V1/V2 and query tiles per CTA (two only for head_dim <= 128).
+// Kernel dispatch on block size, V1/V2, query tiles per CTA (two only for
+// head_dim <= 128) and, for two tiles and bf16, whether V comes from the
+// binary16 copy.
 template <typename T, int D>
-static const void *tc_kernel_ptr(int block_size, bool v1, int tiles)
+static const void *tc_kernel_ptr(int block_size, bool v1, int tiles, bool vh)
 {
 #define PA_PICK(K, BS)                                                                            \
     if (block_size == BS)                                                                         \
         return v1 ? reinterpret_cast<const void *>(&K<T, D, BS, true>)                            \
                   : reinterpret_cast<const void *>(&K<T, D, BS, false>);
+#define PA_PICK_VH(BS)                                                                            \
+    if (block_size == BS)                                                                         \
+        return v1 ? reinterpret_cast<const void *>(&tc2_attn_kernel<T, D, BS, true, true>)        \
+                  : reinterpret_cast<const void *>(&tc2_attn_kernel<T, D, BS, false, true>);
     if (tiles == 2) {
         if constexpr (D <= 128) {
+            if (vh) {
+                if constexpr (Elem<T>::kSplitP) {
+                    PA_PICK_VH(8)
+                    PA_PICK_VH(16)
+                    PA_PICK_VH(32)
+                    PA_PICK_VH(64)
+                }
+                return nullptr;
+            }
             PA_PICK(tc2_attn_kernel, 8)
             PA_PICK(tc2_attn_kernel, 16)
             PA_PICK(tc2_attn_kernel, 32)
@@ -626,6 +644,7 @@ static const void *tc_kernel_ptr(int block_size, bool v1, int tiles)
         }
         return nullptr;
     }
+#undef PA_PICK_VH
     PA_PICK(tc_attn_kernel, 8)
     PA_PICK(tc_attn_kernel, 16)
     PA_PICK(tc_attn_kernel, 32)
@@ -635,9 +654,10 @@ static const void *tc_kernel_ptr(int block_size, bool v1, int tiles)
 }
 
 template <typename T, int D>
-static cudaError_t tc_prepare(int block_size, bool v1, int tiles, int optin_bytes, size_t *limit)
+static cudaError_t tc_prepare(int block_size, bool v1, int tiles, bool vh, int optin_bytes,
+                              size_t *limit)
 {
-    const void *fn = tc_kernel_ptr<T, D>(block_size, v1, tiles);
+    const void *fn = tc_kernel_ptr<T, D>(block_size, v1, tiles, vh);
     if (!fn)
         return cudaErrorInvalidValue;
     cudaFuncAttributes fa;
@@ -653,12 +673,12 @@ static cudaError_t tc_prepare(int block_size, bool v1, int tiles, int optin_byte
 template <typename T, int D>
 static cudaError_t tc_launch(const AttnLaunch &L, cudaStream_t stream)
 {
-    const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1, L.tc_tiles);
+    const void *fn = tc_kernel_ptr<T, D>(L.block_size, L.v1, L.tc_tiles, L.vh);
     if (!fn)
         return cudaErrorInvalidValue;
     // The two-tile kernel also takes the binary16 copy's map (the V map when
     // there is no copy; it is then not read).
-    const CUtensorMap *vh = L.p.vh_flag ? &L.tmap_vh : &L.tmap_v;
+    const CUtensorMap *vh = L.vh ? &L.tmap_vh : &L.tmap_v;
     void *args1[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),
                      const_cast<AttnParams *>(&L.p)};
     void *args2[] = {const_cast<CUtensorMap *>(&L.tmap_k), const_cast<CUtensorMap *>(&L.tmap_v),

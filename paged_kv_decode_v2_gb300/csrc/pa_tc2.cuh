@@ -24,11 +24,11 @@
 // 1 (one row per thread), warp 8 issues the MMAs and owns the TMEM
 // allocation, two lanes of warp 9 load the K and V tiles with TMA.
 //
-// bf16 caches: when the call made a binary16 copy of its V blocks
-// (pa_vhalf.cu) and found no value it cannot hold (*vh_flag == 0), V comes
-// from that copy and P.V runs on binary16 P and V, one MMA per K-step, as
-// for fp16 caches; otherwise P is split into bf16 hi + lo halves.  S = Q K^T
-// stays in bf16.
+// bf16 caches: the VH form reads V from the binary16 copy of the call's V
+// blocks (pa_vhalf.cu) and runs P.V on binary16 P and V, one MMA per K-step,
+// as for fp16 caches; the other form splits P into bf16 hi + lo halves.
+// S = Q K^T stays in bf16.  The host launches the VH form with a fallback
+// behind it, each skipping itself by the copy's flag (AttnParams::skip_if).
 #pragma once
 
 #include "pa_device.cuh"
@@ -49,7 +49,7 @@ struct Tc2Cfg {
     static constexpr uint32_t kSCol = 128;
 };
 
-template <typename T, int D, int BS, bool V1>
+template <typename T, int D, int BS, bool V1, bool VH = false>
 __global__ void __launch_bounds__(kTc2Threads)
     tc2_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
                     const __grid_constant__ CUtensorMap tmap_v,
@@ -77,9 +77,11 @@ __global__ void __launch_bounds__(kTc2Threads)
 
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    // V from the binary16 copy (bf16 caches, copy made and usable): uniform
-    // over the CTA.
-    const bool use_h = kBf16 && p.vh_flag != nullptr && __ldcg(p.vh_flag) == 0;
+    static_assert(!VH || kBf16, "the binary16 copy is for bf16 caches");
+    constexpr bool use_h = VH;
+    // The launch this grid stands in for (or behind) has the work.
+    if (p.skip_if && __ldcg(p.skip_if) == p.skip_val)
+        return;
 
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {

@@ -23,34 +23,51 @@ constexpr int kVhThreads = 256;
 
 __global__ void __launch_bounds__(kVhThreads) v_half_kernel(const VhParams p)
 {
+    __shared__ int s_id[kVhBlocks]; // physical block of each of the CTA's blocks, -1 past the end
     const int s = blockIdx.z;
     const int kv = blockIdx.y;
     const int j0 = blockIdx.x * kVhBlocks;
     int L = __ldg(&p.seq_lens[s]);
     L = L < 0 ? 0 : (L > p.seq_len_cap ? p.seq_len_cap : L);
     const int nb = (L + p.block_size - 1) / p.block_size;
+    if (threadIdx.x < kVhBlocks) {
+        const int j = j0 + threadIdx.x;
+        int id = -1;
+        if (j < nb) {
+            id = __ldg(p.block_tables + (size_t)s * p.max_blocks + j);
+            if (id < 0 || id >= p.num_blocks)
+                id = 0;
+        }
+        s_id[threadIdx.x] = id;
+    }
+    __syncthreads();
     const int per_row = p.head_dim / 8;            // 16-byte chunks of a row
     const int chunks = p.block_size * per_row;     // of one block's slice
     const int total = kVhBlocks * chunks;
-    const int32_t *row = p.block_tables + (size_t)s * p.max_blocks;
-    const uint4 *src = static_cast<const uint4 *>(p.value_cache);
-    uint4 *dst = static_cast<uint4 *>(p.copy) +
-                 (((size_t)s * p.num_kv_heads + kv) * p.max_blocks + j0) * chunks;
+    const uint4 *__restrict__ src = static_cast<const uint4 *>(p.value_cache);
+    uint4 *__restrict__ dst = static_cast<uint4 *>(p.copy) +
+                              (((size_t)s * p.num_kv_heads + kv) * p.max_blocks + j0) * chunks;
     uint32_t big = 0u;
-#pragma unroll 4
-    for (int i = threadIdx.x; i < total; i += kVhThreads) {
-        const int jj = i / chunks;
-        const int c = i - jj * chunks;
-        const int j = j0 + jj;
-        if (j >= nb)
-            continue;
-        int id = __ldg(row + j);
-        if (id < 0 || id >= p.num_blocks)
-            id = 0;
-        uint4 y = make_uint4(0u, 0u, 0u, 0u);
-        if (j * p.block_size + c / per_row < L) {
-            const uint4 x = __ldg(src + ((size_t)id * p.num_kv_heads + kv) * chunks + c);
-            uint32_t w[4] = {x.x, x.y, x.z, x.w};
+    // Four chunks per thread in flight: all loads of a round before any use.
+    for (int base = threadIdx.x; base < total; base += 4 * kVhThreads) {
+        uint4 x[4];
+        int ok[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * kVhThreads;
+            const int jj = i / chunks;
+            const int c = i - jj * chunks;
+            const int id = i < total ? s_id[jj] : -1;
+            // 1: a token row, 0: a row past the sequence's end, -1: a block past it.
+            ok[u] = id < 0 ? -1 : ((j0 + jj) * p.block_size + c / per_row < L ? 1 : 0);
+            x[u] = ok[u] == 1 ? __ldg(src + ((size_t)id * p.num_kv_heads + kv) * chunks + c)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (ok[u] < 0)
+                continue;
+            uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 // Per half: 0x4780 (2^16) <= |bits| < 0x7f80 (inf): finite and too large.
@@ -60,9 +77,8 @@ __global__ void __launch_bounds__(kVhThreads) v_half_kernel(const VhParams p)
                                                     __uint_as_float(w[k] & 0xffff0000u));
                 w[k] = *reinterpret_cast<const uint32_t *>(&h);
             }
-            y = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[base + u * kVhThreads] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        dst[i] = y;
     }
     if (__any_sync(0xffffffffu, big != 0u) && (threadIdx.x & 31) == 0)
         atomicOr(p.flag, 1);
