@@ -290,7 +290,8 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * case below.
  *
  * bf16 caches whose rows take the two-tile tcgen05 kernel (R > 128,
- * head_dim <= 128, max_seq_len >= 1024; pa_set_rows_kernel 0, 2 or 4):
+ * head_dim <= 128, max_seq_len >= 1024; any pa_set_rows_kernel mode but 1, 3
+ * and 6):
  * tmp_output, when given and large enough, also holds a binary16 copy of
  * the V blocks the call reads, and P.V runs on binary16 P and V (one MMA per
  * K-step where bf16 needs a hi + lo pair of P halves).  Layout, in bytes from

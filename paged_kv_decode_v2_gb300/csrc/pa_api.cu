@@ -762,6 +762,50 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
 }
 
 
+// bf16 rows that would take the two-tile kernel under fp16's rule: a binary16
+// copy of the V blocks the call reads, in tmp_output past the partials of
+// np_used partitions (0 for V1), and its flag word; launches the copy pass.
+// vh->copy stays null when the rule does not apply or the copy does not fit.
+int make_v_half_copy(VhCopy *vh, const void *value_cache, const int32_t *block_tables,
+                     const int32_t *seq_lens, int num_seqs, int q_len, int num_heads,
+                     int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                     int max_blocks_per_seq, int cap, float *tmp_output, int max_num_partitions,
+                     int np_used, cudaStream_t stream)
+{
+    const int cols = q_len * (num_heads / num_kv_heads);
+    if (!use_tc(cols) || tc_tiles(cols, head_dim, PA_F16, cap) != 2 || !tmp_output ||
+        !aligned(tmp_output, 16) || max_num_partitions <= 0 || np_used > max_num_partitions)
+        return PA_OK;
+    auto round256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t off = round256((size_t)num_seqs * q_len * num_heads * np_used * head_dim * 4);
+    const size_t copy_bytes =
+        (size_t)num_seqs * num_kv_heads * max_blocks_per_seq * block_size * head_dim * 2;
+    const size_t have =
+        (size_t)num_seqs * q_len * num_heads * (size_t)max_num_partitions * head_dim * 4;
+    const long long rows = (long long)num_seqs * max_blocks_per_seq * num_kv_heads * block_size;
+    if (rows > INT32_MAX || off + round256(copy_bytes) + 256 > have)
+        return PA_OK;
+    char *base = reinterpret_cast<char *>(tmp_output) + off;
+    VhParams vp;
+    vp.value_cache = value_cache;
+    vp.block_tables = block_tables;
+    vp.seq_lens = seq_lens;
+    vp.num_kv_heads = num_kv_heads;
+    vp.head_dim = head_dim;
+    vp.block_size = block_size;
+    vp.num_blocks = num_blocks;
+    vp.max_blocks = max_blocks_per_seq;
+    vp.seq_len_cap = cap;
+    vp.copy = base;
+    vp.flag = reinterpret_cast<int32_t *>(base + round256(copy_bytes));
+    if (cudaMemsetAsync(vp.flag, 0, sizeof(int32_t), stream) != cudaSuccess ||
+        launch_v_half(vp, num_seqs, stream) != cudaSuccess)
+        return PA_ERR_CUDA;
+    vh->copy = vp.copy;
+    vh->flag = vp.flag;
+    return PA_OK;
+}
+
 // V2 for several new tokens (phase 1 and the merge); vh: a binary16 copy of
 // V for the two-tile kernel, or null.
 int v2_mq_impl(const void *query, const void *key_cache, const void *value_cache,
@@ -1033,43 +1077,14 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
         return PA_ERR_INVALID_ARG;
     if (which == 2 && pa_v2_num_partitions(cap, part) > max_num_partitions)
         return PA_ERR_WORKSPACE;
-    // bf16 rows that would take the two-tile kernel as fp16's do: a binary16
-    // copy of the V blocks, in tmp_output past the partials (written at a
-    // stride of the partitions actually used), when it fits.
     VhCopy vh{nullptr, nullptr};
-    int np_used = 0;
-    const int cols = q_len * (num_heads / num_kv_heads);
-    if (dtype == PA_BF16 && use_tc(cols) && tc_tiles(cols, head_dim, PA_F16, cap) == 2 &&
-        tmp_output && aligned(tmp_output, 16) && max_num_partitions > 0) {
-        np_used = which == 2 ? pa_v2_num_partitions(cap, part) : 0;
-        const size_t used = (size_t)num_seqs * q_len * num_heads * np_used * head_dim * 4;
-        const size_t off = (used + 255) & ~(size_t)255;
-        const size_t copy_bytes =
-            (size_t)num_seqs * num_kv_heads * max_blocks_per_seq * block_size * head_dim * 2;
-        const size_t have =
-            (size_t)num_seqs * q_len * num_heads * (size_t)max_num_partitions * head_dim * 4;
-        const long long rows = (long long)num_seqs * max_blocks_per_seq * num_kv_heads * block_size;
-        const size_t need = off + ((copy_bytes + 255) & ~(size_t)255) + 256;
-        if (rows <= INT32_MAX && np_used <= max_num_partitions && need <= have) {
-            char *base = reinterpret_cast<char *>(tmp_output) + off;
-            vh.copy = base;
-            vh.flag = reinterpret_cast<int32_t *>(base + ((copy_bytes + 255) & ~(size_t)255));
-            VhParams vp;
-            vp.value_cache = value_cache;
-            vp.block_tables = block_tables;
-            vp.seq_lens = seq_lens;
-            vp.num_kv_heads = num_kv_heads;
-            vp.head_dim = head_dim;
-            vp.block_size = block_size;
-            vp.num_blocks = num_blocks;
-            vp.max_blocks = max_blocks_per_seq;
-            vp.seq_len_cap = cap;
-            vp.copy = vh.copy;
-            vp.flag = vh.flag;
-            if (cudaMemsetAsync(vh.flag, 0, sizeof(int32_t), st) != cudaSuccess ||
-                launch_v_half(vp, num_seqs, st) != cudaSuccess)
-                return PA_ERR_CUDA;
-        }
+    const int np_used = which == 2 ? pa_v2_num_partitions(cap, part) : 0;
+    if (dtype == PA_BF16) {
+        rc = make_v_half_copy(&vh, value_cache, block_tables, seq_lens, num_seqs, q_len, num_heads,
+                              num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
+                              cap, tmp_output, max_num_partitions, np_used, st);
+        if (rc)
+            return rc;
     }
     const VhCopy *vhp = vh.copy ? &vh : nullptr;
     if (which == 1)
