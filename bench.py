@@ -208,6 +208,121 @@ def recorded_traffic(workload: str, kernel: str):
     return rec.get("dram_bytes_per_launch")
 
 
+# ---------------------------------------------------------------- the read floor
+
+# A plain load kernel over a decode workload's own caches and block table: one
+# CTA per (partition, KV head, sequence) reads the K and V tiles of its blocks
+# (UNROLL blocks per round, every load of a round issued before any is used,
+# nothing computed).  Its time is what reading exactly the decode's bytes in
+# its paged layout costs on this GPU: the floor phase 1 is compared with.
+READ_FLOOR_SRC = r"""
+#include <cstdint>
+#include <cuda_runtime.h>
+template <int UNROLL, int R>
+__global__ void rf_gather(const uint4 *__restrict__ kc, const uint4 *__restrict__ vc,
+                          const int *__restrict__ table, const int *__restrict__ seq_lens,
+                          int max_blocks, int bs, int KV, int bpp, long long pool, unsigned *sink)
+{
+    const int p = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+    const int per = R * blockDim.x;
+    const int L = seq_lens[s];
+    const int nb = (L + bs - 1) / bs;
+    const int b0 = p * bpp;
+    const int b1 = b0 + bpp < nb ? b0 + bpp : nb;
+    const int *row = table + (size_t)s * max_blocks;
+    unsigned acc = 0;
+    for (int b = b0; b < b1; b += UNROLL) {
+        uint4 v[2 * UNROLL * R];
+#pragma unroll
+        for (int k = 0; k < UNROLL; ++k) {
+            const int id = b + k < b1 ? row[b + k] : -1;
+            const bool ok = id >= 0 && id < pool;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const size_t off = ((size_t)(ok ? id : 0) * KV + h) * per + r * blockDim.x + threadIdx.x;
+                v[2 * (k * R + r)] = ok ? __ldcs(kc + off) : make_uint4(0, 0, 0, 0);
+                v[2 * (k * R + r) + 1] = ok ? __ldcs(vc + off) : make_uint4(0, 0, 0, 0);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 2 * UNROLL * R; ++j)
+            acc ^= v[j].x ^ v[j].y ^ v[j].z ^ v[j].w;
+    }
+    if (acc == 0x9e3779b9u)
+        sink[0] = acc;
+}
+extern "C" int rf_launch(const void *kc, const void *vc, const int *table, const int *seq_lens,
+                         int S, int max_blocks, int bs, int KV, int D, int bpp, int np,
+                         long long pool, unsigned *sink, int block, int unroll, void *stream)
+{
+    const int per = bs * D * 2 / 16;
+    if (block <= 0 || per % block || (per / block != 1 && per / block != 2))
+        return 1;
+    dim3 grid(np, KV, S);
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint4 *k = (const uint4 *)kc, *v = (const uint4 *)vc;
+    if (per / block == 1) {
+        if (unroll == 8) rf_gather<8, 1><<<grid, block, 0, st>>>(k, v, table, seq_lens, max_blocks, bs, KV, bpp, pool, sink);
+        else rf_gather<2, 1><<<grid, block, 0, st>>>(k, v, table, seq_lens, max_blocks, bs, KV, bpp, pool, sink);
+    } else {
+        if (unroll == 8) rf_gather<8, 2><<<grid, block, 0, st>>>(k, v, table, seq_lens, max_blocks, bs, KV, bpp, pool, sink);
+        else rf_gather<2, 2><<<grid, block, 0, st>>>(k, v, table, seq_lens, max_blocks, bs, KV, bpp, pool, sink);
+    }
+    return (int)cudaGetLastError();
+}
+"""
+
+
+def read_floor(dec, k1_ms: float) -> dict:
+    """Best time of the plain gather over the workload's caches (a few launch shapes), beside
+    phase 1's time on the same bytes; single-token decode workloads only."""
+    import subprocess
+    w, inp = dec.w, dec.inp
+    build = os.path.join(ROOT, "paged_kv_decode_v2_gb300", "_build")
+    os.makedirs(build, exist_ok=True)
+    src, so = os.path.join(build, "read_floor.cu"), os.path.join(build, "read_floor.so")
+    with open(src, "w") as f:
+        f.write(READ_FLOOR_SRC)
+    subprocess.check_call(["nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared",
+                           "-Xcompiler", "-fPIC", src, "-o", so])
+    lib = ctypes.CDLL(so)
+    V, LL, I = ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int
+    lib.rf_launch.argtypes = [V, V, V, V, I, I, I, I, I, I, I, LL, V, I, I, V]
+    S, maxb = inp.block_tables.shape
+    assert int(inp.seq_lens.max()) <= maxb * w.block_size
+    bpp = max(1, w.partition_size // w.block_size)
+    np_ = -(-dec.max_seq_len // (bpp * w.block_size))
+    per = w.block_size * w.head_dim * 2 // 16
+    sink = torch.zeros(4, dtype=torch.int32, device=dec.device)
+    stream = torch.cuda.current_stream().cuda_stream
+    best = None
+    for block, unroll in ((per, 2), (per // 2, 8), (per, 8), (per // 2, 2)):
+        if not 32 <= block <= 1024:
+            continue
+
+        def fn(k, block=block, unroll=unroll):
+            kc, vc = dec.caches[k % dec.copies]
+            rc = lib.rf_launch(kc.data_ptr(), vc.data_ptr(), inp.block_tables.data_ptr(),
+                               inp.seq_lens.data_ptr(), S, maxb, w.block_size, w.num_kv_heads,
+                               w.head_dim, bpp, np_, inp.key_cache.shape[0], sink.data_ptr(),
+                               block, unroll, stream)
+            if rc:
+                raise RuntimeError(f"read-floor probe launch failed ({rc})")
+        for k in range(5):
+            fn(k)
+        torch.cuda.synchronize()
+        ms = min(time_calls(fn, 5, 50) for _ in range(3))
+        if best is None or ms < best[0]:
+            best = (ms, block, unroll)
+    peak, _ = hbm_peak()
+    gbs = dec.kv_bytes / (best[0] * 1e-3) / 1e9
+    return {"us": round(best[0] * 1e3, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "launch": f"{best[1]} threads, {best[2]} blocks per round",
+            "phase1_over_floor": round(best[0] / k1_ms, 4),
+            "what": "plain loads of the same K/V tiles through the same block table, one CTA per "
+                    "(partition, KV head, sequence), nothing computed"}
+
+
 # ---------------------------------------------------------------- the CUDA path
 
 class Decoder:
@@ -563,6 +678,8 @@ def time_gpu(args, w: wl.Workload):
 
     ms_step, k1_ms, clocks, _ = measure(dec, w, 0, K, W, world, local)
     head = config_line(dec, w, ms_step, k1_ms, clocks, world)
+    if args.read_floor and w.q_len == 1:
+        head["read_floor"] = read_floor(dec, k1_ms)
 
     # End to end through the public API with host buffers: each step copies its
     # inputs (query, block tables, sequence lengths, packed in one pinned
@@ -605,6 +722,8 @@ def time_gpu(args, w: wl.Workload):
         "roofline": head["roofline"],
         "clocks": clocks,
     }
+    if "read_floor" in head:
+        result["read_floor"] = head["read_floor"]
     del host_in
     dec.free()
     del dec
@@ -623,6 +742,8 @@ def time_gpu(args, w: wl.Workload):
             ms_c, k1_c, clk_c, _ = measure(d, wc, 0, PER_CONFIG_STEPS, W, world, local)
             per[name] = config_line(d, wc, ms_c, k1_c, clk_c, world) | {
                 "steps": PER_CONFIG_STEPS, "config": workload_config(d, wc, world)}
+            if args.read_floor and wc.q_len == 1:
+                per[name]["read_floor"] = read_floor(d, k1_c)
             d.free()
             del d
             torch.cuda.empty_cache()
@@ -698,6 +819,10 @@ def main():
                          "kernel up to 8 query rows per KV head)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="time only the chosen workload (no per_config entries)")
+    ap.add_argument("--read-floor", action="store_true",
+                    help="also time a plain load kernel over each decode workload's own caches "
+                         "and block table (built with nvcc on the spot): the read floor that "
+                         "phase 1 is compared with")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
