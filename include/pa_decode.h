@@ -289,9 +289,9 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * coarser) partitioning -- at a stride of max_num_partitions, except in the
  * case below.
  *
- * bf16 caches whose rows take the two-tile tcgen05 kernel (R > 128,
- * head_dim <= 128, max_seq_len >= 1024; any pa_set_rows_kernel mode but 1, 3
- * and 6):
+ * bf16 caches whose rows would take the two-tile tcgen05 kernel under
+ * fp16's rule (R > 128, head_dim <= 128, max_seq_len >= 1024 by default; any
+ * length with pa_set_rows_kernel(4); never with modes 1, 3 and 6):
  * tmp_output, when given and large enough, also holds a binary16 copy of
  * the V blocks the call reads, and P.V runs on binary16 P and V (one MMA per
  * K-step where bf16 needs a hi + lo pair of P halves).  Layout, in bytes from

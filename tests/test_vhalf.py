@@ -172,3 +172,42 @@ def test_bad_block_id_reads_block_zero_and_sets_status():
     out, tmp = run_dispatch(inp, 512, status=status)
     assert int(status.item()) & 1  # PA_STATUS_BAD_BLOCK_ID
     assert torch.isfinite(out).all()
+
+
+def test_copy_with_empty_sequences_mixed_in():
+    """Zero-length sequences between others: no block of theirs is copied or read, and their
+    rows come out zero."""
+    inp = prefill("vh_empty", 40, 4, (0, 1100, 0, 2000, 37), seed=9700)
+    out, tmp = run_dispatch(inp, 512)
+    copy, flag = copy_region(inp, 512, tmp)
+    assert flag == 0
+    check_copy(inp, copy)
+    ref = oracle.decode(oracle_problem(inp))
+    check_out(out, ref, wl.BF16, what="vh_empty")
+    assert (ref[0] == 0).all() and (ref[2] == 0).all()
+
+
+def test_forced_two_tiles_on_short_sequences_use_the_copy(cuda_lib):
+    """pa_set_rows_kernel(4) takes the two-tile kernel, and with it the copy, below 1024 tokens."""
+    cuda_lib.pa_set_rows_kernel(4)
+    inp = prefill("vh_short", 40, 4, (45, 300, 700), seed=9750)
+    out, tmp = run_dispatch(inp, 512)
+    copy, flag = copy_region(inp, 512, tmp)
+    assert flag == 0
+    check_copy(inp, copy)
+    check_out(out, oracle.decode(oracle_problem(inp)), wl.BF16, what="vh_short")
+
+
+def test_one_tile_mode_makes_no_copy(cuda_lib):
+    """pa_set_rows_kernel(3) keeps the one-tile kernel: nothing is written past the partials."""
+    cuda_lib.pa_set_rows_kernel(3)
+    inp = prefill("vh_none", 40, 4, (300, 1100, 2000), seed=9800)
+    out, tmp = run_dispatch(inp, 512)
+    import paged_kv_decode_v2_gb300 as pa
+    S, Q, H, D = inp.query.shape
+    cap = inp.block_tables.shape[1] * 16
+    part = pa.pa_decode_mq_partition(S, Q, H, 2, D, cap, 512)
+    np_used = pa.num_partitions(cap, part) if part > 0 else 0
+    # Partials at the caller's stride (no copy, so no compaction): slots past np_used untouched.
+    assert torch.isnan(tmp[..., np_used:, :]).all()
+    check_out(out, oracle.decode(oracle_problem(inp)), wl.BF16, what="vh_none")
