@@ -374,6 +374,34 @@ class Decoder:
         rows = w.q_len * w.group_size
         self.family = ("pa_tc" if rows >= TC_MIN_ROWS else
                        "pa_simt" if rows <= 8 and ROWS_KERNEL == 5 else "pa_attn")
+        self.vh_copy = w.q_len > 1 and self._makes_v_half_copy(pa, S, H, D)
+        if self.vh_copy:
+            # the copy pass, the two-tile kernel and the one-tile kernel behind it
+            # (which returns at once unless the copy's flag is set), the merge for V2
+            self.launches_per_step = 4 if self.variant == 2 else 3
+
+    def _makes_v_half_copy(self, pa, S, H, D) -> bool:
+        """Whether pa_decode_mq writes the binary16 copy of V for this workload: the rule
+        include/pa_decode.h states (bf16 rows on the two-tile kernel under fp16's rule,
+        and room for the copy in tmp_output past the partials)."""
+        w = self.w
+        rows = w.q_len * w.group_size
+        mode = ROWS_KERNEL
+        uses_tc = mode in (2, 3, 4, 6) or (mode in (0, 5) and rows >= TC_MIN_ROWS)
+        two = D <= 128 and uses_tc and mode not in (3, 6) and (
+            mode == 4 or (rows > 128 and self.max_seq_len >= 1024))
+        if w.dtype != wl.BF16 or not two:
+            return False
+        part = pa.pa_decode_mq_partition(S, w.q_len, H, w.num_kv_heads, D, self.max_seq_len,
+                                         w.partition_size)
+        np_used = pa.num_partitions(self.max_seq_len, part) if self.variant == 2 else 0
+        r256 = lambda x: (x + 255) // 256 * 256
+        maxb = self.inp.block_tables.shape[1]
+        off = r256(S * w.q_len * H * np_used * D * 4)
+        copy = S * w.num_kv_heads * maxb * w.block_size * D * 2
+        have = self.tmp.numel() * 4
+        return (S * maxb * w.num_kv_heads * w.block_size <= 2 ** 31 - 1 and
+                off + r256(copy) + 256 <= have)
 
     def free(self):
         """Drop the device buffers (the caller then empties torch's cache)."""
@@ -758,6 +786,7 @@ def workload_config(dec, w: wl.Workload, world: int):
         "partition_size": w.partition_size, "q_len": w.q_len, "max_seq_len": dec.max_seq_len,
         "sum_seq_len": dec.sum_seq_len, "kv_bytes_per_step": dec.kv_bytes,
         "variant": f"v{dec.variant}", "accumulate": "f32",
+        "binary16_v_copy": bool(getattr(dec, "vh_copy", False)),
         "l2": (f"inputs larger than L2: {dec.copies} rotating K/V cache copies, "
                f"{dec.copies * dec.kv_bytes / 1e6:.0f} MB read between reuses vs 129 MB L2"),
         "parallelism": "replicas" if world > 1 else "single GPU",
