@@ -18,7 +18,8 @@
 
 namespace pa {
 
-constexpr int kVhBlocks = 4;    // blocks of one (sequence, KV head) per CTA
+constexpr int kVhBlocks = 16;   // blocks of one (sequence, KV head) per CTA
+constexpr int kVhRound = 8;     // chunks per thread in flight
 constexpr int kVhThreads = 256;
 
 __global__ void __launch_bounds__(kVhThreads) v_half_kernel(const VhParams p)
@@ -48,12 +49,12 @@ __global__ void __launch_bounds__(kVhThreads) v_half_kernel(const VhParams p)
     uint4 *__restrict__ dst = static_cast<uint4 *>(p.copy) +
                               (((size_t)s * p.num_kv_heads + kv) * p.max_blocks + j0) * chunks;
     uint32_t big = 0u;
-    // Four chunks per thread in flight: all loads of a round before any use.
-    for (int base = threadIdx.x; base < total; base += 4 * kVhThreads) {
-        uint4 x[4];
-        int ok[4];
+    // kVhRound chunks per thread in flight: all loads of a round before any use.
+    for (int base = threadIdx.x; base < total; base += kVhRound * kVhThreads) {
+        uint4 x[kVhRound];
+        int ok[kVhRound];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kVhRound; ++u) {
             const int i = base + u * kVhThreads;
             const int jj = i / chunks;
             const int c = i - jj * chunks;
@@ -64,7 +65,7 @@ __global__ void __launch_bounds__(kVhThreads) v_half_kernel(const VhParams p)
                               : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kVhRound; ++u) {
             if (ok[u] < 0)
                 continue;
             uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
