@@ -376,14 +376,17 @@ class Decoder:
                        "pa_simt" if rows <= 8 and ROWS_KERNEL == 5 else "pa_attn")
         self.vh_copy = w.q_len > 1 and self._makes_v_half_copy(pa, S, H, D)
         if self.vh_copy:
-            # the copy pass, the two-tile kernel and the one-tile kernel behind it
-            # (which returns at once unless the copy's flag is set), the merge for V2
-            self.launches_per_step = 4 if self.variant == 2 else 3
+            # the offsets and copy passes, the two-tile kernel and the one-tile kernel
+            # behind it (which returns at once unless the copy's flag is set), the
+            # merge for V2
+            self.launches_per_step = 5 if self.variant == 2 else 4
 
     def _makes_v_half_copy(self, pa, S, H, D) -> bool:
         """Whether pa_decode_mq writes the binary16 copy of V for this workload: the rule
         include/pa_decode.h states (bf16 rows on the two-tile kernel under fp16's rule,
-        and room for the copy in tmp_output past the partials)."""
+        and room past the partials for the block offsets, the flag and at least one block;
+        whether the packed copy then fits is the device's decision, the launches are the
+        same either way)."""
         w = self.w
         rows = w.q_len * w.group_size
         mode = ROWS_KERNEL
@@ -396,12 +399,9 @@ class Decoder:
                                          w.partition_size)
         np_used = pa.num_partitions(self.max_seq_len, part) if self.variant == 2 else 0
         r256 = lambda x: (x + 255) // 256 * 256
-        maxb = self.inp.block_tables.shape[1]
-        off = r256(S * w.q_len * H * np_used * D * 4)
-        copy = S * w.num_kv_heads * maxb * w.block_size * D * 2
-        have = self.tmp.numel() * 4
-        return (S * maxb * w.num_kv_heads * w.block_size <= 2 ** 31 - 1 and
-                off + r256(copy) + 256 <= have)
+        off = r256(S * w.q_len * H * np_used * D * 4) + r256(4 * (S + 1))
+        block = w.num_kv_heads * w.block_size * D * 2
+        return off + block <= self.tmp.numel() * 4
 
     def free(self):
         """Drop the device buffers (the caller then empties torch's cache)."""

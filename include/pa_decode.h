@@ -290,27 +290,32 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * case below.
  *
  * bf16 caches whose rows would take the two-tile tcgen05 kernel under
- * fp16's rule (R > 128, head_dim <= 128, max_seq_len >= 1024 by default; any
- * length with pa_set_rows_kernel(4); never with modes 1, 3 and 6):
- * tmp_output, when given and large enough, also holds a binary16 copy of
- * the V blocks the call reads, and P.V runs on binary16 P and V (one MMA per
- * K-step where bf16 needs a hi + lo pair of P halves).  Layout, in bytes from
- * tmp_output: the partials at a stride of the partitions used (np, 0 for
- * V1), num_seqs * q_len * num_heads * np * head_dim * 4 bytes; at the next
- * multiple of 256 the copy, [num_seqs][num_kv_heads][max_blocks_per_seq]
- * [block_size][head_dim] binary16 (a sequence's logical block j at index
- * j, rows past its end zero, an out-of-range block id read as block 0); at
- * the next multiple of 256 after it a 32-bit flag, set to 1 when a finite
- * value of magnitude 2^16 or more was met (binary16 cannot hold it): the
- * call then reads the bf16 cache with P in hi + lo halves instead (the
- * binary16 kernel and a one-tile bf16 kernel are both launched; each reads
- * the flag first and one of them returns at once).  Every
- * bf16 value below 2^16 has an exact binary16 form, so the copy loses
- * nothing.  When tmp_output (num_seqs * q_len * num_heads *
- * max_num_partitions * head_dim * 4 bytes) cannot hold all three, or the
- * copy's rows exceed 2^31, there is no copy and the call runs the one-tile
- * kernel with hi + lo P.  The copy adds one read and one write of the V
- * blocks' bytes to the call.
+ * fp16's rule (R > 128, head_dim <= 128, max_seq_len >= 1024), with R >=
+ * 1024 (any R and length with pa_set_rows_kernel(4); never with modes 1, 3
+ * and 6): tmp_output, when large enough, also holds a binary16 copy of the
+ * V blocks the call reads, and P.V runs on binary16 P and V (one MMA per
+ * K-step where bf16 needs a hi + lo pair of P halves).  Below 1024 rows per
+ * KV head the copy's extra read and write of V outweighs what it saves.
+ * Layout, in bytes from tmp_output (num_seqs * q_len * num_heads *
+ * max_num_partitions * head_dim * 4 bytes in all): the partials at a stride
+ * of the partitions used (np, 0 for V1), num_seqs * q_len * num_heads * np *
+ * head_dim * 4 bytes; at the next multiple of 256, num_seqs 32-bit block
+ * offsets, offs[s] = the sum of ceil(L_t / block_size) over t < s with L_t
+ * clamped to the capacity, and a 32-bit flag after them; at the next
+ * multiple of 256 after the flag the copy, [num_kv_heads][copy_blocks]
+ * [block_size][head_dim] binary16, copy_blocks as many as the rest of
+ * tmp_output holds (at most 2^31 rows in all): a sequence's logical block j
+ * at index offs[s] + j of each KV head's part, rows past its end zero, an
+ * out-of-range block id read as block 0.  The flag is set to 1 when the
+ * sequences' blocks do not fit copy_blocks (the lengths are device data) or
+ * a finite value of magnitude 2^16 or more was met (binary16 cannot hold
+ * it): the call then reads the bf16 cache with P in hi + lo halves instead
+ * (the binary16 kernel and a one-tile bf16 kernel are both launched; each
+ * reads the flag first and one of them returns at once).  Every bf16 value
+ * below 2^16 has an exact binary16 form, so the copy loses nothing.  When
+ * tmp_output cannot hold the offsets, the flag and one block, there is no
+ * copy and the call runs the one-tile kernel with hi + lo P.  The copy adds
+ * one read and one write of the V blocks' bytes to the call.
  */
 PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *value_cache,
                         const int32_t *block_tables, const int32_t *seq_lens, int num_seqs,

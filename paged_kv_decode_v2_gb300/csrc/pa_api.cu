@@ -21,6 +21,8 @@ constexpr int kMaxDevices = 64;
 struct VhCopy {
     void *copy;
     int32_t *flag;
+    const int32_t *offs;         // each sequence's first block in the packed copy
+    int copy_blocks;             // blocks the copy's space holds
 };
 
 std::atomic<int> g_tune_warps{0};
@@ -446,10 +448,14 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     if (vh) {
         // The copy is [S][KV][max_blocks][block_size][head_dim] binary16: the
         // cache map's shape with S * max_blocks blocks.
-        rc = encode_cache_map(&L.tmap_vh, vh->copy, PA_F16, num_seqs * max_blocks_per_seq,
-                              num_kv_heads, block_size, head_dim);
+        rc = encode_cache_map(&L.tmap_vh, vh->copy, PA_F16, vh->copy_blocks, num_kv_heads,
+                              block_size, head_dim);
         if (rc)
             return rc;
+    }
+    if (vh) {
+        L.p.vh_offs = vh->offs;
+        L.p.vh_blocks = vh->copy_blocks;
     }
     // With the binary16 copy, bf16 rows take the kernel fp16's would.
     const int tile_dtype = vh ? PA_F16 : dtype;
@@ -762,10 +768,16 @@ int choose_variant_mq(int num_seqs, int q_len, int group, int num_kv_heads, int 
 }
 
 
-// bf16 rows that would take the two-tile kernel under fp16's rule: a binary16
-// copy of the V blocks the call reads, in tmp_output past the partials of
-// np_used partitions (0 for V1), and its flag word; launches the copy pass.
-// vh->copy stays null when the rule does not apply or the copy does not fit.
+// bf16 rows that would take the two-tile kernel under fp16's rule, kVhMinRows
+// or more of them per KV head (any number when pa_set_rows_kernel(4) forces
+// two tiles): a binary16 copy of the V blocks the call reads, packed per KV
+// head, in tmp_output past the
+// partials of np_used partitions (0 for V1): the per-sequence block offsets
+// and the flag word at the next multiple of 256 bytes, the copy at the next
+// multiple of 256 after them, filling the rest of tmp_output.  The offsets
+// pass sets the flag when the packed copy does not fit (lengths are device
+// data); the attention kernels then read the bf16 cache.  vh->copy stays null
+// when the rule does not apply or not even the offsets fit.
 int make_v_half_copy(VhCopy *vh, const void *value_cache, const int32_t *block_tables,
                      const int32_t *seq_lens, int num_seqs, int q_len, int num_heads,
                      int num_kv_heads, int head_dim, int num_blocks, int block_size,
@@ -773,36 +785,52 @@ int make_v_half_copy(VhCopy *vh, const void *value_cache, const int32_t *block_t
                      int np_used, cudaStream_t stream)
 {
     const int cols = q_len * (num_heads / num_kv_heads);
-    if (!use_tc(cols) || tc_tiles(cols, head_dim, PA_F16, cap) != 2 || !tmp_output ||
+    const bool forced = g_rows_kernel.load(std::memory_order_relaxed) == 4;
+    if (!use_tc(cols) || tc_tiles(cols, head_dim, PA_F16, cap) != 2 ||
+        (cols < kVhMinRows && !forced) || !tmp_output ||
         !aligned(tmp_output, 16) || max_num_partitions <= 0 || np_used > max_num_partitions)
         return PA_OK;
     auto round256 = [](size_t x) { return (x + 255) & ~(size_t)255; };
     const size_t off = round256((size_t)num_seqs * q_len * num_heads * np_used * head_dim * 4);
-    const size_t copy_bytes =
-        (size_t)num_seqs * num_kv_heads * max_blocks_per_seq * block_size * head_dim * 2;
+    const size_t copy_off = off + round256((size_t)(num_seqs + 1) * 4);
     const size_t have =
         (size_t)num_seqs * q_len * num_heads * (size_t)max_num_partitions * head_dim * 4;
-    const long long rows = (long long)num_seqs * max_blocks_per_seq * num_kv_heads * block_size;
-    if (rows > INT32_MAX || off + round256(copy_bytes) + 256 > have)
+    const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * 2;
+    if (copy_off + block_bytes > have)
         return PA_OK;
-    char *base = reinterpret_cast<char *>(tmp_output) + off;
+    // Blocks the space holds, kept within 32-bit TMA row coordinates.
+    long long copy_blocks = (long long)((have - copy_off) / block_bytes);
+    const long long max_rows_blocks = (long long)INT32_MAX / ((long long)num_kv_heads * block_size);
+    if (copy_blocks > max_rows_blocks)
+        copy_blocks = max_rows_blocks;
+    char *base = reinterpret_cast<char *>(tmp_output);
     VhParams vp;
     vp.value_cache = value_cache;
     vp.block_tables = block_tables;
     vp.seq_lens = seq_lens;
+    vp.num_seqs = num_seqs;
     vp.num_kv_heads = num_kv_heads;
     vp.head_dim = head_dim;
     vp.block_size = block_size;
     vp.num_blocks = num_blocks;
     vp.max_blocks = max_blocks_per_seq;
     vp.seq_len_cap = cap;
-    vp.copy = base;
-    vp.flag = reinterpret_cast<int32_t *>(base + round256(copy_bytes));
-    if (cudaMemsetAsync(vp.flag, 0, sizeof(int32_t), stream) != cudaSuccess ||
-        launch_v_half(vp, num_seqs, stream) != cudaSuccess)
+    vp.copy_blocks = copy_blocks;
+    vp.offs = reinterpret_cast<int32_t *>(base + off);
+    vp.flag = vp.offs + num_seqs;
+    vp.copy = base + copy_off;
+    int dev;
+    if (current_device(&dev))
+        return PA_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return PA_ERR_CUDA;
+    if (launch_v_half(vp, sms, stream) != cudaSuccess)
         return PA_ERR_CUDA;
     vh->copy = vp.copy;
     vh->flag = vp.flag;
+    vh->offs = vp.offs;
+    vh->copy_blocks = (int)copy_blocks;
     return PA_OK;
 }
 
@@ -1077,7 +1105,7 @@ PA_API int pa_decode_mq(const void *query, const void *key_cache, const void *va
         return PA_ERR_INVALID_ARG;
     if (which == 2 && pa_v2_num_partitions(cap, part) > max_num_partitions)
         return PA_ERR_WORKSPACE;
-    VhCopy vh{nullptr, nullptr};
+    VhCopy vh{nullptr, nullptr, nullptr, 0};
     const int np_used = which == 2 ? pa_v2_num_partitions(cap, part) : 0;
     if (dtype == PA_BF16) {
         rc = make_v_half_copy(&vh, value_cache, block_tables, seq_lens, num_seqs, q_len, num_heads,

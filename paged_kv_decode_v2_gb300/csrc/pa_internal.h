@@ -50,6 +50,8 @@ struct AttnParams {
     int32_t *counters;           // fused V2: [S, KV] tickets, zero between calls
     const int32_t *skip_if;      // when non-null: the grid does nothing if *skip_if == skip_val
     int skip_val;
+    const int32_t *vh_offs;      // binary16 copy of V: each sequence's first block in it
+    int vh_blocks;               // and the blocks one KV head's part of it holds
     int32_t *status;
 };
 
@@ -89,22 +91,34 @@ struct MergeParams {
 };
 
 // The binary16 copy of the V blocks a multi-query call reads (bf16 caches):
-// [S][KV][max_blocks][block_size][head_dim], rows past a sequence's end zero,
-// and a flag word set when a finite value is 2^16 or more in magnitude.
+// the blocks the sequences use, packed -- sequence s's logical block j at
+// index offs[s] + j of a [blocks][KV][block_size][head_dim] array (offs the
+// exclusive prefix sum of ceil(L_s / block_size)), rows past a sequence's
+// end zero -- and a flag word, 1 when the copy is not to be used: a finite
+// value of 2^16 or more in magnitude, or more blocks than `copy_blocks`.
 struct VhParams {
     const void *value_cache;
     const int32_t *block_tables;
     const int32_t *seq_lens;
+    int num_seqs;
     int num_kv_heads;
     int head_dim;
     int block_size;
     int num_blocks;
     int max_blocks;
     int seq_len_cap;
+    long long copy_blocks;       // blocks the copy's space holds
+    int32_t *offs;               // [num_seqs], written by the offsets pass
     void *copy;
     int32_t *flag;
 };
-cudaError_t launch_v_half(const VhParams &p, int num_seqs, cudaStream_t stream);
+cudaError_t launch_v_half(const VhParams &p, int num_sms, cudaStream_t stream);
+// Query rows per KV head below which the copy is not made (unless
+// pa_set_rows_kernel(4) forces the two-tile kernel): the copy costs one read
+// and one write of the V blocks whatever the rows, while the binary16 P.V it
+// enables saves MMA work in proportion to them.  On uniform batches of 1 to
+// 8192 tokens it paid from 1024 rows per KV head and lost at 256.
+constexpr int kVhMinRows = 1024;
 
 // Per-warp shared-memory ring bytes for one stage: a K tile and a V tile of
 // block_size rows (at least 16: an 8-token block size stages two blocks) x

@@ -24,8 +24,8 @@
 // 1 (one row per thread), warp 8 issues the MMAs and owns the TMEM
 // allocation, two lanes of warp 9 load the K and V tiles with TMA.
 //
-// bf16 caches: the VH form reads V from the binary16 copy of the call's V
-// blocks (pa_vhalf.cu) and runs P.V on binary16 P and V, one MMA per K-step,
+// bf16 caches: the VH form reads V from the packed binary16 copy of the
+// call's V blocks (pa_vhalf.cu) and runs P.V on binary16 P and V, one MMA per K-step,
 // as for fp16 caches; the other form splits P into bf16 hi + lo halves.
 // S = Q K^T stays in bf16.  The host launches the VH form with a fallback
 // behind it, each skipping itself by the copy's flag (AttnParams::skip_if).
@@ -204,9 +204,10 @@ __global__ void __launch_bounds__(kTc2Threads)
         if (lane < 2) {
             const bool is_k = lane == 0;
             const CUtensorMap *map = is_k ? &tmap_k : use_h ? &tmap_vh : &tmap_v;
-            // Row of block k of tile t in the binary16 copy: the sequence's
-            // logical block blk0 + t * kBPT + k.
-            const long long vh_row0 = ((long long)b * p.num_kv_heads + kv) * p.max_blocks + blk0;
+            // The binary16 copy, [KV][vh_blocks][block_size] rows, holds the
+            // sequence's logical block j of KV head kv at kv * vh_blocks + vh_offs[b] + j.
+            const long long vh_blk0 =
+                use_h ? (long long)kv * p.vh_blocks + __ldg(&p.vh_offs[b]) + blk0 : 0;
             const uint32_t ring = is_k ? k_sm : v_sm;
             const uint32_t full = is_k ? b_k_full : b_v_full;
             const uint32_t empty = is_k ? b_k_empty : b_v_empty;
@@ -249,8 +250,9 @@ __global__ void __launch_bounds__(kTc2Threads)
                 for (int k = 0; k < kBPT; ++k) {
                     if (k < nb) {
                         const int row =
-                            !is_k && use_h ? (int)((vh_row0 + t * kBPT + k) * BS)
-                                           : (int)(((long long)ids[k] * p.num_kv_heads + kv) * BS);
+                            !is_k && use_h
+                                ? (int)((vh_blk0 + t * kBPT + k) * BS)
+                                : (int)(((long long)ids[k] * p.num_kv_heads + kv) * BS);
 #pragma unroll
                         for (int sl = 0; sl < C::kSlices; ++sl)
                             tma_load_3d(ring + s * C::kKVBytes + sl * C::kKVSlice + k * BS * 128, map,

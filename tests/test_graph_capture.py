@@ -5,7 +5,7 @@ on the caller's stream, allocates nothing and never synchronises, so a capture
 holds the whole call (tensor maps are encoded on the host at capture time).
 Covered: the single-token dispatch (V2 with the merge), the multi-query
 dispatch on the tcgen05 kernel, and the bf16 path through the binary16 copy of
-V (a memset node, the copy pass, two attention kernels and the merge).
+V (the offsets pass, the copy pass, two attention kernels and the merge).
 """
 import pytest
 import torch
@@ -62,9 +62,11 @@ def test_single_token_dispatch_in_a_graph():
     captured_equals_eager(run)
 
 
-@pytest.mark.parametrize("q_len,G,dtype", [(16, 4, wl.BF16), (40, 4, wl.BF16), (40, 4, wl.F16)])
+@pytest.mark.parametrize("q_len,G,dtype", [(16, 4, wl.BF16), (40, 4, wl.BF16), (40, 4, wl.F16),
+                                           (256, 4, wl.BF16)])
 def test_multi_query_dispatch_in_a_graph(q_len, G, dtype):
-    """64 rows (one-tile V2), and 160 rows: two tiles, through the binary16 copy for bf16."""
+    """64 rows (one-tile V2); 160 rows: two tiles for fp16, one with hi + lo P for bf16; 1024
+    bf16 rows: two tiles through the binary16 copy."""
     import paged_kv_decode_v2_gb300 as pa
     inp = wl.make_inputs(mq("graph_mq", q_len, G, (300, 1100, 2000), P=512, dtype=dtype,
                             seed=9950 + q_len + dtype), device="cuda")

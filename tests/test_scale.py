@@ -71,7 +71,7 @@ def test_single_token(cuda_lib, scale, entry):
 @pytest.mark.parametrize("q_len,G,mode,dtype", [(4, 4, 0, wl.BF16),     # 16 rows: mma.sync
                                                (16, 4, 3, wl.BF16),    # 64 rows: one tile, half Q
                                                (40, 4, 4, wl.F16),     # 160 rows: two tiles
-                                               (40, 4, 0, wl.BF16)])   # bf16 via the binary16 copy
+                                               (40, 4, 4, wl.BF16)])   # bf16 via the binary16 copy
 def test_multi_query(cuda_lib, scale, q_len, G, mode, dtype):
     import paged_kv_decode_v2_gb300 as pa
     cuda_lib.pa_set_rows_kernel(mode)
