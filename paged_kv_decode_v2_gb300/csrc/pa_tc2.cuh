@@ -412,8 +412,9 @@ __global__ void __launch_bounds__(kTc2Threads)
                     tmem_ld_wait(sr[k]);
                 if (whole) {
 #pragma unroll
-                    for (int c = 0; c < kTc2Tok; ++c)
-                        mq[c & 3] = fmaxf(mq[c & 3], __uint_as_float(sr[c >> 5][c & 31]));
+                    for (int c = 0; c < kTc2Tok; c += 2)
+                        mq[(c >> 1) & 3] = fmax3(mq[(c >> 1) & 3], __uint_as_float(sr[c >> 5][c & 31]),
+                                                 __uint_as_float(sr[c >> 5][(c & 31) + 1]));
                 } else {
 #pragma unroll
                     for (int c = 0; c < kTc2Tok; ++c) {
@@ -443,6 +444,8 @@ __global__ void __launch_bounds__(kTc2Threads)
             // the S columns just read: per 32 tokens, hi halves at [32k, 32k +
             // 16), lo at [32k + 16, 32k + 32).
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            uint64_t ls2[2] = {0ull, 0ull}; // packed row sums of the binary16 form
+            const uint64_t cf2 = f2_pack(cf, cf), nmb2 = f2_pack(-mb, -mb);
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 uint32_t sr[2][32];
@@ -480,15 +483,20 @@ __global__ void __launch_bounds__(kTc2Threads)
                         // binary16 P: fp16 caches, or bf16 with V from the copy
 #pragma unroll
                         for (int c = 0; c < 32; c += 2) {
-                            const float x0 = __uint_as_float(sr[k][c]), x1 = __uint_as_float(sr[k][c + 1]);
-                            const float p0 = fast_exp2(fmaf(x0, cf, -mb));
-                            const float p1 = fast_exp2(fmaf(x1, cf, -mb));
-                            ls[(c >> 1) & 3] += p0 + p1;
+                            float y0, y1;
+                            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[k][c]), __uint_as_float(sr[k][c + 1])),
+                                             cf2, nmb2),
+                                      y0, y1);
+                            const float p0 = fast_exp2(y0), p1 = fast_exp2(y1);
+                            ls2[(c >> 1) & 1] = f2_add(ls2[(c >> 1) & 1], f2_pack(p0, p1));
                             ph[c >> 1] = Elem<__half>::pack(p0, p1);
                         }
                         tmem_st16(col, ph);
                     }
                 }
+            }
+            if (!(kBf16 && !use_h)) {
+                f2_unpack(f2_add(ls2[0], ls2[1]), ls[0], ls[1]);
             }
             l_run = fmaf(l_run, a, (ls[0] + ls[1]) + (ls[2] + ls[3]));
             // Rescale O when m moved (O holds P.V of earlier tiles only from t = 1).
