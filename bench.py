@@ -376,10 +376,9 @@ class Decoder:
                        "pa_simt" if rows <= 8 and ROWS_KERNEL == 5 else "pa_attn")
         self.vh_copy = w.q_len > 1 and self._makes_v_half_copy(pa, S, H, D)
         if self.vh_copy:
-            # the offsets and copy passes, the two-tile kernel and the one-tile kernel
-            # behind it (which returns at once unless the copy's flag is set), the
-            # merge for V2
-            self.launches_per_step = 5 if self.variant == 2 else 4
+            # the offsets and copy passes, the two-tile kernel (binary16 or, when the
+            # copy's flag is set, bf16 P), the merge for V2
+            self.launches_per_step = 4 if self.variant == 2 else 3
 
     def _makes_v_half_copy(self, pa, S, H, D) -> bool:
         """Whether pa_decode_mq writes the binary16 copy of V for this workload: the rule

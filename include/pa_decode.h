@@ -310,8 +310,8 @@ PA_API int pa_decode_mq_partition(int num_seqs, int q_len, int num_heads, int nu
  * sequences' blocks do not fit copy_blocks (the lengths are device data) or
  * a finite value of magnitude 2^16 or more was met (binary16 cannot hold
  * it): the call then reads the bf16 cache with P in hi + lo halves instead
- * (the binary16 kernel and a one-tile bf16 kernel are both launched; each
- * reads the flag first and one of them returns at once).  Every bf16 value
+ * (the attention kernel reads the flag once the copy pass has completed and
+ * takes its bf16 form, still on two tiles).  Every bf16 value
  * below 2^16 has an exact binary16 form, so the copy loses nothing.  When
  * tmp_output cannot hold the offsets, the flag and one block, there is no
  * copy and the call runs the one-tile kernel with hi + lo P.  The copy adds

@@ -446,16 +446,15 @@ int build_attn(AttnLaunch &L, const void *query, const void *key_cache, const vo
     if (rc)
         return rc;
     if (vh) {
-        // The copy is [S][KV][max_blocks][block_size][head_dim] binary16: the
-        // cache map's shape with S * max_blocks blocks.
+        // The copy is [KV][copy_blocks][block_size][head_dim] binary16: as rows,
+        // the cache map's shape with copy_blocks blocks.
         rc = encode_cache_map(&L.tmap_vh, vh->copy, PA_F16, vh->copy_blocks, num_kv_heads,
                               block_size, head_dim);
         if (rc)
             return rc;
-    }
-    if (vh) {
         L.p.vh_offs = vh->offs;
         L.p.vh_blocks = vh->copy_blocks;
+        L.p.vh_flag = vh->flag;
     }
     // With the binary16 copy, bf16 rows take the kernel fp16's would.
     const int tile_dtype = vh ? PA_F16 : dtype;
@@ -558,25 +557,7 @@ int v2_phase1_impl(const void *query, const void *key_cache, const void *value_c
                     max_num_partitions, fused_out, status, counters, vh);
     if (rc)
         return rc;
-    if (!L.vh)
-        return prepare_and_launch_attn(L, stream);
-    // The binary16 form, then the bf16 form behind it: each does the work or
-    // nothing, by the copy's flag (set: a value the copy cannot hold).
-    L.p.skip_if = vh->flag;
-    L.p.skip_val = 1;
-    rc = prepare_and_launch_attn(L, stream);
-    if (rc)
-        return rc;
-    AttnLaunch F;
-    rc = build_attn(F, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
-                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
-                    cap, scale, dtype, false, np, partition_size, tmp_output, exp_sums, max_logits,
-                    max_num_partitions, fused_out, status, counters, nullptr);
-    if (rc)
-        return rc;
-    F.p.skip_if = vh->flag;
-    F.p.skip_val = 0;
-    return prepare_and_launch_attn(F, stream);
+    return prepare_and_launch_attn(L, stream);
 }
 
 int v2_phase2_impl(const int32_t *seq_lens, int num_seqs, int q_len, int num_heads, int head_dim,
@@ -883,23 +864,7 @@ int v1_mq_impl(const void *query, const void *key_cache, const void *value_cache
                     nullptr, vh);
     if (rc)
         return rc;
-    if (!L.vh)
-        return prepare_and_launch_attn(L, stream);
-    // As in v2_phase1_impl: the binary16 form, then the bf16 form behind it.
-    L.p.skip_if = vh->flag;
-    L.p.skip_val = 1;
-    rc = prepare_and_launch_attn(L, stream);
-    if (rc)
-        return rc;
-    AttnLaunch F;
-    rc = build_attn(F, query, key_cache, value_cache, block_tables, seq_lens, num_seqs, q_len,
-                    num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_blocks_per_seq,
-                    cap, scale, dtype, true, 1, 0, nullptr, nullptr, nullptr, 0, out, status);
-    if (rc)
-        return rc;
-    F.p.skip_if = vh->flag;
-    F.p.skip_val = 0;
-    return prepare_and_launch_attn(F, stream);
+    return prepare_and_launch_attn(L, stream);
 }
 
 } // namespace

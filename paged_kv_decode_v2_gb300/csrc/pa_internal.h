@@ -48,8 +48,7 @@ struct AttnParams {
     float *max_logits;           // V2: [S, q_len, H, NPcap]
     void *out;                   // V1 and fused V2: [S, q_len, H, D]
     int32_t *counters;           // fused V2: [S, KV] tickets, zero between calls
-    const int32_t *skip_if;      // when non-null: the grid does nothing if *skip_if == skip_val
-    int skip_val;
+    const int32_t *vh_flag;      // binary16 copy of V: its flag, 0 when the copy holds V
     const int32_t *vh_offs;      // binary16 copy of V: each sequence's first block in it
     int vh_blocks;               // and the blocks one KV head's part of it holds
     int32_t *status;

@@ -95,9 +95,6 @@ __global__ void __launch_bounds__(kTcThreads, D <= 128 ? 2 : 1)
     // the previous grid in the stream has completed.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;");
-    // A fallback launch whose work another grid has done (AttnParams::skip_if).
-    if (p.skip_if && __ldcg(p.skip_if) == p.skip_val)
-        return;
 
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {

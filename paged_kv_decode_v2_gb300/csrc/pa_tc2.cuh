@@ -27,8 +27,8 @@
 // bf16 caches: the VH form reads V from the packed binary16 copy of the
 // call's V blocks (pa_vhalf.cu) and runs P.V on binary16 P and V, one MMA per K-step,
 // as for fp16 caches; the other form splits P into bf16 hi + lo halves.
-// S = Q K^T stays in bf16.  The host launches the VH form with a fallback
-// behind it, each skipping itself by the copy's flag (AttnParams::skip_if).
+// S = Q K^T stays in bf16.  The VH kernel holds both forms and takes the bf16
+// one when the copy's flag is set.
 #pragma once
 
 #include "pa_device.cuh"
@@ -49,11 +49,11 @@ struct Tc2Cfg {
     static constexpr uint32_t kSCol = 128;
 };
 
-template <typename T, int D, int BS, bool V1, bool VH = false>
-__global__ void __launch_bounds__(kTc2Threads)
-    tc2_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                    const __grid_constant__ CUtensorMap tmap_v,
-                    const __grid_constant__ CUtensorMap tmap_vh, const AttnParams p)
+// The kernel's body for one P format: H, V from the binary16 copy and P in
+// binary16 (bf16 caches only); otherwise the cache's own form.
+template <typename T, int D, int BS, bool V1, bool H>
+__device__ __forceinline__ void tc2_body(const CUtensorMap &tmap_k, const CUtensorMap &tmap_v,
+                                         const CUtensorMap &tmap_vh, const AttnParams &p)
 {
     static_assert(D <= 128, "two query tiles need O + S of each in 256 TMEM columns");
     using C = Tc2Cfg<D>;
@@ -75,13 +75,8 @@ __global__ void __launch_bounds__(kTc2Threads)
     const int kv = blockIdx.y;
     const int b = blockIdx.z;
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;");
-    static_assert(!VH || kBf16, "the binary16 copy is for bf16 caches");
-    constexpr bool use_h = VH;
-    // The launch this grid stands in for (or behind) has the work.
-    if (p.skip_if && __ldcg(p.skip_if) == p.skip_val)
-        return;
+    static_assert(!H || kBf16, "the binary16 copy is for bf16 caches");
+    constexpr bool use_h = H;
 
     int L = __ldg(&p.seq_lens[b]);
     if (L < 0 || L > p.seq_len_cap) {
@@ -597,6 +592,30 @@ __global__ void __launch_bounds__(kTc2Threads)
     if (warp == 8) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// VH = false: the form of the cache's type.  VH = true (bf16): V from the
+// binary16 copy with binary16 P, unless the copy's flag is set (a value
+// binary16 cannot hold, or a copy too large for its space), in which case the
+// bf16 form with hi + lo P on the cache; the flag is final once the previous
+// grid (the copy pass) has completed, so every thread reads the same value.
+template <typename T, int D, int BS, bool V1, bool VH = false>
+__global__ void __launch_bounds__(kTc2Threads)
+    tc2_attn_kernel(const __grid_constant__ CUtensorMap tmap_k,
+                    const __grid_constant__ CUtensorMap tmap_v,
+                    const __grid_constant__ CUtensorMap tmap_vh,
+                    const __grid_constant__ AttnParams p)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;");
+    if constexpr (VH) {
+        if (__ldcg(p.vh_flag) == 0)
+            tc2_body<T, D, BS, V1, true>(tmap_k, tmap_v, tmap_vh, p);
+        else
+            tc2_body<T, D, BS, V1, false>(tmap_k, tmap_v, tmap_vh, p);
+    } else {
+        tc2_body<T, D, BS, V1, false>(tmap_k, tmap_v, tmap_vh, p);
     }
 }
 

@@ -5,7 +5,7 @@ on the caller's stream, allocates nothing and never synchronises, so a capture
 holds the whole call (tensor maps are encoded on the host at capture time).
 Covered: the single-token dispatch (V2 with the merge), the multi-query
 dispatch on the tcgen05 kernel, and the bf16 path through the binary16 copy of
-V (the offsets pass, the copy pass, two attention kernels and the merge).
+V (the offsets pass, the copy pass, the attention kernel and the merge).
 """
 import pytest
 import torch
