@@ -183,3 +183,24 @@ def check_mq(inp, P, entries=("v2", "v1")):
 def mq(name, q_len, G, lens, bs=16, P=64, dtype=wl.BF16, D=128, KV=2, seed=0):
     return wl.Workload(name, len(lens), G * KV, KV, D, bs, P, dtype, "list", seq_lens=tuple(lens),
                        q_len=q_len, seed=seed)
+
+
+def ramp_scores(inp, c, period=None):
+    """Add c * position (modulo period) to dimension 0 of every key and set dimension 0 of the queries
+    to +1 for even heads and -1 for odd ones: scores rise by ~c * scale per token on even heads and
+    fall on odd heads, so rows of one warp disagree on whether their running max moves."""
+    w = inp.workload
+    bs = w.block_size
+    q = inp.query
+    sign = torch.ones(w.num_heads, device=q.device)
+    sign[1::2] = -1.0
+    q[..., 0] = sign.to(q.dtype)
+    lens = inp.seq_lens.tolist()
+    for b, L in enumerate(lens):
+        nb = -(-L // bs)
+        ids = inp.block_tables[b, :nb].long()
+        pos = torch.arange(nb * bs, device=q.device, dtype=torch.float32).view(nb, 1, bs)
+        if period:
+            pos = pos % period
+        inp.key_cache[ids, :, :, 0] = (c * pos).expand(nb, w.num_kv_heads, bs).to(inp.key_cache.dtype)
+    return inp

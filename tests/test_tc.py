@@ -19,7 +19,7 @@ import torch
 
 import oracle
 import workloads as wl
-from parity_util import (OUT_ABS, check_mq, check_out, check_partitions, half_ulp, mq,
+from parity_util import (OUT_ABS, check_mq, check_out, check_partitions, half_ulp, mq, ramp_scores,
                          oracle_problem, run_mq, run_v2)
 
 pytestmark = pytest.mark.gpu
@@ -141,35 +141,16 @@ def test_tc_values_beyond_binary16(dtype):
         assert (err <= tol).all(), (e, int((err > tol).sum()), float((err - tol).max()))
 
 
-def ramp_scores(inp, c, period=None):
-    """Add c * position (modulo period) to dimension 0 of every key and set dimension 0 of the queries
-    to +1 for even heads and -1 for odd ones: scores rise by ~c * scale per token on even heads and
-    fall on odd heads, so rows of one warp disagree on whether their running max moves."""
-    w = inp.workload
-    bs = w.block_size
-    q = inp.query
-    sign = torch.ones(w.num_heads, device=q.device)
-    sign[1::2] = -1.0
-    q[..., 0] = sign.to(q.dtype)
-    lens = inp.seq_lens.tolist()
-    for b, L in enumerate(lens):
-        nb = -(-L // bs)
-        ids = inp.block_tables[b, :nb].long()
-        pos = torch.arange(nb * bs, device=q.device, dtype=torch.float32).view(nb, 1, bs)
-        if period:
-            pos = pos % period
-        inp.key_cache[ids, :, :, 0] = (c * pos).expand(nb, w.num_kv_heads, bs).to(inp.key_cache.dtype)
-    return inp
-
-
+@pytest.mark.parametrize("dtype", [wl.BF16, wl.F16])
 @pytest.mark.parametrize("c,period", [(1.5, None), (0.3, None), (4.0, 256)])
-def test_tc_rising_and_falling_scores(c, period):
+def test_tc_rising_and_falling_scores(c, period, dtype):
     """On half the rows the running max grows past the rescale threshold every tile (c = 1.5), every
     few tiles (c = 0.3), or by ~22 per tile for four tiles and then repeats without growing (c = 4,
     period 256); on the others it never grows.  O is rescaled for some rows of a warp and not the
     rest; V2's partition statistics still report the true max.  Logits stay below ~130, where fp32
-    scores keep the exp_sums tolerance."""
-    w = mq("tc_ramp", 8, 4, (700, 300, 1000, 65), P=256, seed=8900 + int(10 * c))
+    scores keep the exp_sums tolerance.  fp16 as well as bf16, so that every P format runs the ramps
+    (fp16 on two tiles: binary16 P, ~5, ~24 and ~65 in exp2 terms per 128-token tile)."""
+    w = mq("tc_ramp", 8, 4, (700, 300, 1000, 65), P=256, dtype=dtype, seed=8900 + int(10 * c) + dtype)
     inp = ramp_scores(wl.make_inputs(w, device="cuda"), c, period)
     check_mq(inp, 256)
 

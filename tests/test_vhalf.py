@@ -18,7 +18,7 @@ import torch
 
 import oracle
 import workloads as wl
-from parity_util import OUT_ABS, check_out, half_ulp, mq, oracle_problem
+from parity_util import OUT_ABS, check_out, half_ulp, mq, oracle_problem, ramp_scores
 
 pytestmark = pytest.mark.gpu
 
@@ -263,6 +263,20 @@ def test_forced_two_tiles_on_short_sequences_use_the_copy(cuda_lib):
     assert flag == 0
     check_copy(inp, copy, offs)
     check_out(out, oracle.decode(oracle_problem(inp)), wl.BF16, what="vh_short")
+
+
+@pytest.mark.parametrize("c,period", [(1.5, None), (0.3, None), (4.0, 256)])
+def test_copy_with_rising_and_falling_scores(cuda_lib, c, period):
+    """pa_set_rows_kernel(4), 160 rows, scores rising on half the heads (the tcgen05 suite's ramps):
+    through the copy, with binary16 P, the lazy rescale of O and l still matches the oracle."""
+    cuda_lib.pa_set_rows_kernel(4)
+    inp = ramp_scores(prefill("vh_ramp", 40, 4, (700, 300, 1000, 65), seed=9720 + int(10 * c)), c,
+                      period)
+    out, tmp = run_dispatch(inp, 512)
+    copy, offs, flag = copy_region(inp, 512, tmp)
+    assert flag == 0
+    check_copy(inp, copy, offs)
+    check_out(out, oracle.decode(oracle_problem(inp)), wl.BF16, what=f"vh_ramp c={c}")
 
 
 def test_one_tile_mode_makes_no_copy(cuda_lib):
