@@ -62,6 +62,8 @@ KERNEL_SOURCES = {
 }
 # From this many query rows per KV head the library runs the tcgen05 kernel.
 TC_MIN_ROWS = 32
+# From this many (bf16, two tiles) it writes the binary16 copy of V.
+VH_MIN_ROWS = 1024
 # pa_set_rows_kernel mode of this run (--rows-kernel).
 ROWS_KERNEL = 0
 
@@ -392,7 +394,8 @@ class Decoder:
         uses_tc = mode in (2, 3, 4, 6) or (mode in (0, 5) and rows >= TC_MIN_ROWS)
         two = D <= 128 and uses_tc and mode not in (3, 6) and (
             mode == 4 or (rows > 128 and self.max_seq_len >= 1024))
-        if w.dtype != wl.BF16 or not two:
+        # 1024 rows per KV head at least, unless mode 4 forces two tiles
+        if w.dtype != wl.BF16 or not two or (rows < VH_MIN_ROWS and mode != 4):
             return False
         part = pa.pa_decode_mq_partition(S, w.q_len, H, w.num_kv_heads, D, self.max_seq_len,
                                          w.partition_size)
