@@ -486,10 +486,14 @@ __device__ __forceinline__ void tc2_body(const CUtensorMap &tmap_k, const CUtens
                             ls2[(c >> 1) & 1] = f2_add(ls2[(c >> 1) & 1], f2_pack(p0, p1));
                             ph[c >> 1] = Elem<__half>::pack(p0, p1);
                         }
-                        tmem_st16(col, ph);
+                        tmem_st16_async(col, ph);
                     }
                 }
             }
+            // One wait for the tile's P stores (tcgen05.st takes its registers
+            // when issued), before the arrival below lets P.V read them.
+            if (!(kBf16 && !use_h))
+                tmem_st_wait();
             if (!(kBf16 && !use_h)) {
                 f2_unpack(f2_add(ls2[0], ls2[1]), ls[0], ls[1]);
             }
