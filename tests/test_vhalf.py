@@ -160,6 +160,38 @@ def test_values_beyond_binary16_set_the_flag():
     assert (np.abs(o - ref) <= OUT_ABS + half_ulp(ref, wl.BF16) + 2.0 ** -11 * ref_abs).all()
 
 
+def test_values_beyond_binary16_on_the_v1_path():
+    """The V1 shape of test_copy_on_the_v1_path with one value of 2^16 or more: the flag is set
+    and the two-tile kernel takes its bf16 form (hi + lo P on the cache) in the same launch."""
+    import paged_kv_decode_v2_gb300 as pa
+    lens = tuple(1100 + 37 * i for i in range(6))
+    inp = prefill("vh_v1_wide", 128, 8, lens, KV=8, seed=9460)
+    S, Q, H, D = inp.query.shape
+    cap = inp.block_tables.shape[1] * 16
+    assert pa.pa_decode_mq_choose(S, Q, H, 8, D, cap, 512) == 1
+    t = 777
+    inp.value_cache[int(inp.block_tables.cpu()[2, t // 16]), 5, t % 16, 9] = -9.0e4
+    out, tmp = run_dispatch(inp, 512)
+    assert copy_region(inp, 512, tmp)[2] == 1
+    arrays = wl.to_oracle_arrays(inp)
+    ref = oracle.decode(oracle.Problem.from_arrays(arrays))
+    arrays["value_cache"] = arrays["value_cache"] & np.uint16(0x7FFF)
+    ref_abs = oracle.decode(oracle.Problem.from_arrays(arrays))
+    o = out.cpu().to(torch.float64).numpy()
+    assert np.isfinite(o).all()
+    assert (np.abs(o - ref) <= OUT_ABS + half_ulp(ref, wl.BF16) + 2.0 ** -11 * ref_abs).all()
+
+
+def test_copy_path_is_reproducible():
+    """Three calls on the same inputs through the copy (offsets pass, copy pass, two-tile kernel,
+    merge) give bitwise the same output."""
+    inp = prefill("vh_repro", QL, GR, (300, 1100, 2000), seed=9560)
+    first, _ = run_dispatch(inp, 512)
+    for _ in range(2):
+        again, _ = run_dispatch(inp, 512)
+        assert torch.equal(first, again)
+
+
 def test_poison_does_not_set_the_flag():
     """NaN in every slot the call must not read (unreferenced blocks, rows past each sequence's
     end) changes nothing, bit for bit, and leaves the flag clear."""
