@@ -397,9 +397,10 @@ PA_API int pa_set_rows_kernel(int mode);
 
 /*
  * Form of phase 2 (the merge), process-wide: 0 (default) by rule -- one warp
- * per (row, head) when the longest sequence has at most 8 partitions and
- * there are more than 16 (row, head) pairs per SM, else one CTA per (head,
- * row, slice of head_dim); 1 always the CTA-per-slice form; 2 always the
+ * per (row, head) when there are more than 16 (row, head) pairs per SM and
+ * the longest sequence has at most 8 partitions, or at most 32 with 32 pairs
+ * per SM or more; else one CTA per (head, row, slice of head_dim); 1 always
+ * the CTA-per-slice form; 2 always the
  * warp-per-pair form (up to 2^30 pairs, else the CTA form).  Both fold the
  * partitions with the same rule; the choice changes only speed.  Returns
  * PA_ERR_INVALID_ARG for other values.  A tuning and test hook, with no

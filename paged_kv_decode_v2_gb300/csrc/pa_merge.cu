@@ -242,10 +242,20 @@ int merge_form(const MergeParams &p, int num_seqs, int num_sms, int forced)
     const long long pairs = (long long)p.num_heads * num_seqs * p.q_len;
     if (forced == 1 || (forced == 2 && pairs <= (1LL << 30)))
         return forced;
-    // Row form when every sequence has at most 8 partitions and the slice
-    // form would launch more than 16 CTAs per SM.
+    // Row form when the slice form would launch more than 16 CTAs per SM and
+    // every sequence has at most 8 partitions, or, from 32 pairs per SM, at
+    // most 32: the slice form's CTA per pair leaves most of its lanes idle
+    // when a batch's pairs have few partitions each, and the row form's warps
+    // take a long pair's partitions one after another.  Measured on GB300 (us
+    // per call, slice / row form): ragged batch (64 sequences, lognormal
+    // lengths to 32K) with 2, 4, 8, 16 new tokens 144.8 / 140.4, 197.7 /
+    // 187.3, 220.3 / 196.4, 285.3 / 237.4 (16 to 32 partitions, 8K to 64K
+    // pairs); the same batch with one new token 142.5 / 143.6 (64 partitions,
+    // 4K pairs); one 100K-token sequence 37.1 / 69.7; stress at 2 sequences
+    // 159.5 / 179.0.
     const int np_max = (p.seq_len_cap + p.partition_size - 1) / p.partition_size;
-    return np_max <= 8 && pairs > 16LL * num_sms && pairs <= (1LL << 30) ? 2 : 1;
+    const bool many = pairs > 16LL * num_sms && pairs <= (1LL << 30);
+    return many && (np_max <= 8 || (np_max <= 32 && pairs >= 32LL * num_sms)) ? 2 : 1;
 }
 
 cudaError_t launch_merge(int dtype, const MergeParams &p, int num_seqs, int num_sms, int form,

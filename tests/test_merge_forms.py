@@ -68,3 +68,22 @@ def test_merge_form_rule(cuda_lib):
     cuda_lib.pa_set_merge_form(2)
     out2 = run_mq(inp, 512, entry="v2")[0].clone()
     assert torch.equal(out0, out2)
+
+
+@pytest.mark.parametrize("longest,form", [(20 * 512, 2), (40 * 512, 1)])
+def test_merge_form_rule_partition_bound(cuda_lib, longest, form):
+    """From 32 pairs per SM the default takes the warp-per-pair form up to 32 partitions at the
+    longest (20 here) and the CTA-per-slice form beyond (40); its output equals that form's bit for
+    bit."""
+    from parity_util import run_mq
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S, Q, G, KV = 20, 8, 4, 8
+    assert S * Q * G * KV >= 32 * sms
+    lens = tuple(max(Q, longest - 997 * i) for i in range(S))
+    w = mq("merge_bound", Q, G, lens, P=512, KV=KV, seed=9350 + longest // 512)
+    inp = wl.make_inputs(w, device="cuda")
+    cuda_lib.pa_set_merge_form(0)
+    out0 = run_mq(inp, 512, entry="v2")[0].clone()
+    cuda_lib.pa_set_merge_form(form)
+    outf = run_mq(inp, 512, entry="v2")[0].clone()
+    assert torch.equal(out0, outf)
